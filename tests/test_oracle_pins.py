@@ -136,7 +136,17 @@ def test_bitval_outside_mask_is_ignored():
         b = [int(v) for v in rng.integers(0, 2**32, W, dtype=np.uint64)]
         x = [bm & mm if rng.random() < 0.7 else int(rng.integers(0, 2**32)) for bm, mm in zip(b, m)]
         bin_ = [bb & mm for bb, mm in zip(b, m)]
-        assert R.compress_row(x, m, b) == R.compress_row(x, m, bin_)
+        slot, comp, used = R.compress_row(x, m, b)
+        assert (slot, comp, used) == R.compress_row(x, m, bin_)
+        # Bitval bits outside the Mask never reach a decoded word either
+        assert R.decode_row(slot, comp, m, b) == (R.OK, x)
+    rows = np.random.default_rng(2).integers(0, 2**32, (64, 40), dtype=np.uint64).astype(np.uint32)
+    m = rows[0] & rows[1]
+    b = rows[2]
+    rows[::2] = (rows[::2] & ~m) | (b & m)
+    slots, bitmask, _ = C.compress(rows, m, b)
+    st, back = C.decompress(slots, bitmask, np.arange(64), m, b)
+    assert st == 0 and np.array_equal(back, rows)
 
 
 # ---------------------------------------------------------------------------
