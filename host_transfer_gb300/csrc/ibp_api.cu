@@ -1,0 +1,377 @@
+// ibp_api.cu - the C ABI of libibp: argument checks, pointer resolution,
+// plan lifetime, status word.  Kernels live in the other .cu files.
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cmath>
+#include <new>
+
+#include "ibp_internal.cuh"
+
+namespace ibp {
+
+static thread_local char g_detail[256] = "";
+
+void set_cuda_error(cudaError_t e, const char* where) {
+  snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+}
+
+int check_launch(const char* where) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_cuda_error(e, where);
+    return IBP_ECUDA;
+  }
+  return IBP_OK;
+}
+
+int resolve_ptr(const void* p, int device, const void** dev) {
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return IBP_EINVAL;
+  }
+  switch (attr.type) {
+    case cudaMemoryTypeDevice:
+      if (attr.device != device) return IBP_EINVAL;
+      *dev = p;
+      return IBP_OK;
+    case cudaMemoryTypeManaged:
+      *dev = p;
+      return IBP_OK;
+    case cudaMemoryTypeHost:
+      if (attr.devicePointer == nullptr) return IBP_EINVAL;
+      *dev = attr.devicePointer;
+      return IBP_OK;
+    default:
+      return IBP_EINVAL;  // pageable host memory
+  }
+}
+
+int sm_count(int device) {
+  static int cached[64] = {0};
+  if (device >= 0 && device < 64 && cached[device]) return cached[device];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 1;
+  }
+  if (device >= 0 && device < 64) cached[device] = n;
+  return n;
+}
+
+// Makes `device` current for the lifetime of the guard.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int device) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      set_cuda_error(cudaGetLastError(), "cudaGetDevice");
+      return;
+    }
+    if (prev != device) {
+      cudaError_t e = cudaSetDevice(device);
+      if (e != cudaSuccess) {
+        ok = false;
+        set_cuda_error(e, "cudaSetDevice");
+        cudaGetLastError();
+      }
+    }
+  }
+  ~DeviceGuard() {
+    if (ok && prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace ibp
+
+using namespace ibp;
+
+extern "C" {
+
+const char* ibp_strerror(int status) {
+  switch (status) {
+    case IBP_OK: return "IBP_OK: success";
+    case IBP_EINVAL: return "IBP_EINVAL: invalid argument";
+    case IBP_ECUDA: return "IBP_ECUDA: CUDA runtime error";
+    case IBP_ENOMEM: return "IBP_ENOMEM: device allocation failed";
+    case IBP_ECORRUPT: return "IBP_ECORRUPT: corrupt compressed slot";
+    case IBP_ERANGE: return "IBP_ERANGE: row id out of range";
+    case IBP_ETIMEOUT: return "IBP_ETIMEOUT: bounded wait expired";
+    default: return "IBP_?: unknown status";
+  }
+}
+
+int ibp_version(void) { return IBP_VERSION; }
+
+const char* ibp_last_error_detail(void) { return g_detail; }
+
+int ibp_preprocess(const uint32_t* sample, uint64_t s_rows, uint32_t W, double T, uint32_t* mask,
+                   uint32_t* bitval, void* stream) {
+  g_detail[0] = 0;
+  if (W == 0 || W > IBP_MAX_W || s_rows == 0 || s_rows >= (1ull << 32)) return IBP_EINVAL;
+  if (!(T > 0.0 && T <= 1.0)) return IBP_EINVAL;
+  if (!sample || !mask || !bitval) return IBP_EINVAL;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    set_cuda_error(cudaGetLastError(), "cudaGetDevice");
+    return IBP_ECUDA;
+  }
+  const void *ds, *dm, *db;
+  if (resolve_ptr(sample, device, &ds) || resolve_ptr(mask, device, &dm) ||
+      resolve_ptr(bitval, device, &db))
+    return IBP_EINVAL;
+  return launch_preprocess(static_cast<const uint32_t*>(ds), s_rows, W, T,
+                           const_cast<uint32_t*>(static_cast<const uint32_t*>(dm)),
+                           const_cast<uint32_t*>(static_cast<const uint32_t*>(db)),
+                           static_cast<cudaStream_t>(stream));
+}
+
+int ibp_plan_create(const uint32_t* mask, const uint32_t* bitval, uint32_t W, int device,
+                    ibp_plan** out) {
+  g_detail[0] = 0;
+  if (!out || !mask || !bitval || W == 0 || W > IBP_MAX_W) return IBP_EINVAL;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+    set_cuda_error(cudaGetLastError(), "cudaGetDeviceCount");
+    return IBP_ECUDA;
+  }
+  if (device < 0 || device >= ndev) return IBP_EINVAL;
+  DeviceGuard g(device);
+  if (!g.ok) return IBP_ECUDA;
+
+  ibp_plan* p = new (std::nothrow) ibp_plan();
+  if (!p) return IBP_ENOMEM;
+  p->device = device;
+  p->W = W;
+  p->S = (W + 31) / 32;
+  // Layout (words): mask, bm, pcnt, rmask[4], rshift, mv[5] = 13 W; planes 6 S;
+  // status 1 (padded to 4).
+  const size_t words = 13ull * W + 6ull * p->S + 4;
+  p->d_bytes = words * 4;
+  cudaError_t e = cudaMalloc(&p->d_block, p->d_bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return IBP_ENOMEM;
+  }
+  uint32_t* base = static_cast<uint32_t*>(p->d_block);
+  PlanView& v = p->view;
+  v.W = W;
+  v.S = p->S;
+  v.mask = base;
+  v.bm = base + 1ull * W;
+  v.pcnt = base + 2ull * W;
+  v.rmask = base + 3ull * W;
+  v.rshift = base + 7ull * W;
+  v.mv = base + 8ull * W;
+  v.planes = base + 13ull * W;
+  v.status = base + 13ull * W + 6ull * p->S;
+  // Mask and Bitval go to the mask and bm slots; the table kernel cleans bm.
+  e = cudaMemcpy(const_cast<uint32_t*>(v.mask), mask, 4ull * W, cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemcpy(const_cast<uint32_t*>(v.bm), bitval, 4ull * W, cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemset(v.status, 0, 4);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "ibp_plan_create copy");
+    cudaGetLastError();
+    cudaFree(p->d_block);
+    delete p;
+    return IBP_ECUDA;
+  }
+  int rc = build_plan_tables(p);
+  if (rc != IBP_OK) {
+    cudaFree(p->d_block);
+    delete p;
+    return rc;
+  }
+  *out = p;
+  return IBP_OK;
+}
+
+int ibp_plan_destroy(ibp_plan* plan) {
+  if (!plan) return IBP_OK;
+  DeviceGuard g(plan->device);
+  cudaError_t e = cudaFree(plan->d_block);
+  delete plan;
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "cudaFree");
+    return IBP_ECUDA;
+  }
+  return IBP_OK;
+}
+
+int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out) {
+  if (!plan || !out) return IBP_EINVAL;
+  out->W = plan->W;
+  out->segments = plan->S;
+  out->uniform = plan->uniform;
+  out->max_runs = plan->max_runs;
+  out->min_kept_bits = plan->min_kept;
+  out->max_kept_bits = plan->max_kept;
+  out->metadata_bytes = plan->d_bytes;
+  out->device = plan->device;
+  return IBP_OK;
+}
+
+int ibp_plan_get_mask(const ibp_plan* plan, uint32_t* mask, uint32_t* bitval) {
+  if (!plan) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  cudaError_t e = cudaSuccess;
+  if (mask) e = cudaMemcpy(mask, plan->view.mask, 4ull * plan->W, cudaMemcpyDefault);
+  if (e == cudaSuccess && bitval)
+    e = cudaMemcpy(bitval, plan->view.bm, 4ull * plan->W, cudaMemcpyDefault);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "ibp_plan_get_mask");
+    cudaGetLastError();
+    return IBP_ECUDA;
+  }
+  return IBP_OK;
+}
+
+int ibp_compress(const ibp_plan* plan, const uint32_t* rows, uint32_t* slots, uint64_t n_rows,
+                 uint32_t* bitmask, uint64_t* stored_words, void* stream) {
+  g_detail[0] = 0;
+  if (!plan) return IBP_EINVAL;
+  if (n_rows == 0) return IBP_OK;
+  if (!rows || !slots || !bitmask) return IBP_EINVAL;
+  const uint64_t W = plan->W;
+  if (n_rows > (~0ull) / (4 * W)) return IBP_EINVAL;
+  // in place, or no overlap at all
+  const uintptr_t r0 = reinterpret_cast<uintptr_t>(rows), s0 = reinterpret_cast<uintptr_t>(slots);
+  const uintptr_t len = n_rows * W * 4;
+  if (r0 != s0 && r0 < s0 + len && s0 < r0 + len) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void *dr, *ds, *db, *dst = nullptr;
+  if (resolve_ptr(rows, plan->device, &dr) || resolve_ptr(slots, plan->device, &ds) ||
+      resolve_ptr(bitmask, plan->device, &db))
+    return IBP_EINVAL;
+  if (stored_words && resolve_ptr(stored_words, plan->device, &dst)) return IBP_EINVAL;
+  CompressArgs a;
+  a.pv = plan->view;
+  a.rows = static_cast<const uint32_t*>(dr);
+  a.slots = const_cast<uint32_t*>(static_cast<const uint32_t*>(ds));
+  a.n_rows = n_rows;
+  a.bitmask = const_cast<uint32_t*>(static_cast<const uint32_t*>(db));
+  a.stored = const_cast<unsigned long long*>(static_cast<const unsigned long long*>(dst));
+  a.vec = (W % 4 == 0) && aligned16(a.rows) && aligned16(a.slots);
+  a.rowcap = static_cast<uint32_t>(((W + 3) / 4) * 4 + 4);
+  return launch_compress(plan, a, static_cast<cudaStream_t>(stream));
+}
+
+static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                             const uint32_t* bitmask, const int64_t* ids, uint64_t first,
+                             uint64_t n_out, uint32_t* out, void* stream) {
+  const uint64_t W = plan->W;
+  if (n_rows > (~0ull) / (4 * W) || n_out > (~0ull) / (4 * W)) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void *dsl, *dbm, *dout, *dids = nullptr;
+  if (resolve_ptr(slots, plan->device, &dsl) || resolve_ptr(bitmask, plan->device, &dbm) ||
+      resolve_ptr(out, plan->device, &dout))
+    return IBP_EINVAL;
+  if (ids && resolve_ptr(ids, plan->device, &dids)) return IBP_EINVAL;
+  DecodeArgs a;
+  a.pv = plan->view;
+  a.slots = static_cast<const uint32_t*>(dsl);
+  a.bitmask = static_cast<const uint32_t*>(dbm);
+  a.ids = static_cast<const int64_t*>(dids);
+  a.first = first;
+  a.n_rows = n_rows;
+  a.n_out = n_out;
+  a.out = const_cast<uint32_t*>(static_cast<const uint32_t*>(dout));
+  a.vec = (W % 4 == 0) && aligned16(a.slots) && aligned16(a.out);
+  a.rowcap = static_cast<uint32_t>(((W + 3) / 4) * 4 + 4);
+  a.scap = ((plan->S + 3) / 4) * 4;
+  uint32_t G = 1152u / a.rowcap;
+  a.G = G < 1 ? 1 : (G > 32 ? 32 : G);
+  return launch_decompress(plan, a, static_cast<cudaStream_t>(stream));
+}
+
+int ibp_gather_decompress(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                          const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
+                          uint32_t* out, void* stream) {
+  g_detail[0] = 0;
+  if (!plan) return IBP_EINVAL;
+  if (n_ids == 0) return IBP_OK;
+  if (!slots || !bitmask || !row_ids || !out || n_rows == 0) return IBP_EINVAL;
+  return decompress_common(plan, slots, n_rows, bitmask, row_ids, 0, n_ids, out, stream);
+}
+
+int ibp_decompress_contig(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                          const uint32_t* bitmask, uint64_t first_row, uint64_t n, uint32_t* out,
+                          void* stream) {
+  g_detail[0] = 0;
+  if (!plan) return IBP_EINVAL;
+  if (n == 0) return IBP_OK;
+  if (!slots || !bitmask || !out) return IBP_EINVAL;
+  if (first_row >= n_rows || n > n_rows - first_row) return IBP_EINVAL;
+  return decompress_common(plan, slots, n_rows, bitmask, nullptr, first_row, n, out, stream);
+}
+
+int ibp_get_status(const ibp_plan* plan, void* stream) {
+  g_detail[0] = 0;
+  if (!plan) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  uint32_t st = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&st, plan->view.status, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && st != 0) e = cudaMemset(plan->view.status, 0, 4);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "ibp_get_status");
+    cudaGetLastError();
+    return IBP_ECUDA;
+  }
+  return static_cast<int>(st);
+}
+
+int ibp_row_lengths(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                    const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
+                    uint32_t* lengths, void* stream) {
+  g_detail[0] = 0;
+  if (!plan) return IBP_EINVAL;
+  if (n_ids == 0) return IBP_OK;
+  if (!slots || !bitmask || !row_ids || !lengths || n_rows == 0) return IBP_EINVAL;
+  if (n_rows > (~0ull) / (4ull * plan->W) || n_ids > (1ull << 40)) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void *ds, *db, *di, *dl;
+  if (resolve_ptr(slots, plan->device, &ds) || resolve_ptr(bitmask, plan->device, &db) ||
+      resolve_ptr(row_ids, plan->device, &di) || resolve_ptr(lengths, plan->device, &dl))
+    return IBP_EINVAL;
+  return launch_row_lengths(plan, static_cast<const uint32_t*>(ds), n_rows,
+                            static_cast<const uint32_t*>(db), static_cast<const int64_t*>(di), n_ids,
+                            const_cast<uint32_t*>(static_cast<const uint32_t*>(dl)),
+                            static_cast<cudaStream_t>(stream));
+}
+
+int ibp_gather_raw(const uint32_t* rows, uint64_t n_rows, uint32_t W, const int64_t* row_ids,
+                   uint64_t n_ids, uint32_t* out, void* stream) {
+  g_detail[0] = 0;
+  if (W == 0 || W > IBP_MAX_W) return IBP_EINVAL;
+  if (n_ids == 0) return IBP_OK;
+  if (!rows || !row_ids || !out || n_rows == 0) return IBP_EINVAL;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    set_cuda_error(cudaGetLastError(), "cudaGetDevice");
+    return IBP_ECUDA;
+  }
+  const void *dr, *di, *dout;
+  if (resolve_ptr(rows, device, &dr) || resolve_ptr(row_ids, device, &di) ||
+      resolve_ptr(out, device, &dout))
+    return IBP_EINVAL;
+  const bool vec = (W % 4 == 0) && aligned16(dr) && aligned16(dout);
+  return launch_gather_raw(static_cast<const uint32_t*>(dr), n_rows, W,
+                           static_cast<const int64_t*>(di), n_ids,
+                           const_cast<uint32_t*>(static_cast<const uint32_t*>(dout)), vec, device,
+                           static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

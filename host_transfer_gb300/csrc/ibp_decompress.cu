@@ -1,0 +1,349 @@
+// ibp_decompress.cu - warp-parallel gather-decompress of IBP slots.
+//
+// « Algorithme central », step 3 (Décompression): a warp of 32 threads
+// cooperatively reads a contiguous compressed segment from CPU memory into a
+// shared-memory workspace; warp primitives give each thread the starting bit
+// offset of the word it owns; each thread rebuilds its word by putting the
+// Bitval bits back at the Mask positions; asynchronous memory accesses
+// overlap the fetch of later rows with the decoding of the current ones.
+// « Intégration au système »: only the compressed prefix of a fixed-size slot
+// is read, and a bitmask in GPU memory says which rows are compressed.
+//
+// GB300 design.  Each warp owns groups of G consecutive output rows (G = 32
+// for 32-word rows down to 1 for rows of 1 K words and more) and runs a
+// three-deep software pipeline over its groups:
+//   ids of group j+3 -> registers            (plain loads)
+//   headers of group j+2 -> shared memory     (cp.async, 16 B)
+//   payload of group j+1 -> shared memory     (cp.async, 16 B, only the
+//                                              compressed prefix)
+//   decode of group j: one lane per word, 32 words per step
+// so a warp keeps the payload of G rows plus the headers of G more rows in
+// flight while it decodes.  cp.async reads mapped pinned host memory and HBM
+// alike.  Offsets: when every word position has the same Mask the offset of
+// lane i within a segment is 32 i - p * popc(H & lanemask_lt) (p = popcount
+// of the Mask); otherwise a 5-step shuffle scan of the per-word field
+// lengths.  Reinsertion: y = deposit(v) | (Bitval & Mask) with deposit done by
+// up to four precomputed runs of kept bits, or by the five-step parallel-
+// suffix expand for masks with more runs.
+#include <cuda_runtime.h>
+
+#include "ibp_internal.cuh"
+
+namespace ibp {
+
+constexpr int kDecWarpsMax = 8;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+template <bool UNIFORM, int R>
+__device__ __forceinline__ uint32_t rebuild_word(const PlanView& pv, uint32_t v, uint32_t w) {
+  if constexpr (UNIFORM) {
+    if constexpr (R > 0) return deposit_runs<R>(v, pv.u_rmask, pv.u_rsh) | pv.u_bm;
+    return expand5(v, pv.u_mv, pv.u_keep) | pv.u_bm;
+  } else {
+    const uint32_t W = pv.W;
+    if constexpr (R > 0) {
+      uint32_t rm[R], rs[R];
+      const uint32_t sh = __ldg(pv.rshift + w);
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+        rm[k] = __ldg(pv.rmask + k * W + w);
+        rs[k] = (sh >> (8 * k)) & 0xFFu;
+      }
+      return deposit_runs<R>(v, rm, rs) | __ldg(pv.bm + w);
+    }
+    uint32_t mv[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) mv[i] = __ldg(pv.mv + i * W + w);
+    return expand5(v, mv, ~__ldg(pv.mask + w)) | __ldg(pv.bm + w);
+  }
+}
+
+// Decode one compressed row whose stream words [S, Lw) are in pb and whose
+// S header words are in hb; write its W words to orow.
+template <bool UNIFORM, int R>
+__device__ __forceinline__ void decode_row(const PlanView& pv, const uint32_t* __restrict__ pb,
+                                           const uint32_t* __restrict__ hb,
+                                           uint32_t* __restrict__ orow, uint32_t lane) {
+  const uint32_t W = pv.W, S = pv.S;
+  const uint32_t lt = lanemask_lt();
+  uint32_t base = 32u * S;  // stream bit of segment s's first field
+  for (uint32_t s = 0; s < S; ++s) {
+    const uint32_t H = hb[s];
+    const uint32_t w = 32u * s + lane;
+    const uint32_t flag = (H >> lane) & 1u;
+    uint32_t off, seg;
+    if constexpr (UNIFORM) {
+      const uint32_t nwords = min(32u, W - 32u * s);
+      off = 32u * lane - pv.u_p * __popc(H & lt);
+      seg = 32u * nwords - pv.u_p * __popc(H);
+    } else {
+      const uint32_t len = (w < W) ? (flag ? 32u - __ldg(pv.pcnt + w) : 32u) : 0u;
+      uint32_t incl = len;
+#pragma unroll
+      for (uint32_t d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl += t;
+      }
+      off = incl - len;
+      seg = __shfl_sync(kFull, incl, 31);
+    }
+    if (w < W) {
+      const uint32_t P = base + off;
+      const uint32_t lo = pb[P >> 5];
+      const uint32_t hi = pb[(P >> 5) + 1];
+      const uint32_t v = __funnelshift_r(lo, hi, P & 31u);
+      orow[w] = flag ? rebuild_word<UNIFORM, R>(pv, v, w) : v;
+    }
+    base += seg;
+  }
+}
+
+template <bool UNIFORM, int R>
+__global__ void __launch_bounds__(kDecWarpsMax * 32) k_decompress(const DecodeArgs a) {
+  extern __shared__ __align__(16) uint32_t smem[];
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t nw_cta = blockDim.x >> 5;
+  const uint32_t G = a.G, W = a.pv.W, S = a.pv.S;
+  const uint32_t rowcap = a.rowcap, scap = a.scap;
+  uint32_t* const pbuf = smem + warp * (2u * G * rowcap + 3u * G * scap);  // [2][G][rowcap]
+  uint32_t* const hbuf = pbuf + 2u * G * rowcap;                           // [3][G][scap]
+
+  const uint64_t n_groups = (a.n_out + G - 1) / G;
+  const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw_cta + warp;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw_cta;
+  if (gw >= n_groups) return;  // warp-uniform; only warp-level syncs below
+  const uint64_t J = (n_groups - gw + nwarps - 1) / nwarps;
+
+  // Lane q < G of group j owns output row (gw + j * nwarps) * G + q.
+  auto row_index = [&](uint64_t j) -> uint64_t { return (gw + j * nwarps) * G + lane; };
+  auto present = [&](uint64_t j) -> bool { return j < J && lane < G && row_index(j) < a.n_out; };
+
+  auto load_id = [&](uint64_t j) -> int64_t {
+    if (!present(j)) return -1;
+    const uint64_t i = row_index(j);
+    return a.ids ? a.ids[i] : static_cast<int64_t>(a.first + i);
+  };
+
+  auto in_table = [&](int64_t id) -> bool {
+    return id >= 0 && static_cast<uint64_t>(id) < a.n_rows;
+  };
+
+  // Headers of group j -> hbuf[hs]; the row's bitmask word -> bmw.
+  auto issue_headers = [&](uint64_t j, uint32_t hs, int64_t id, uint32_t& bmw) {
+    const bool ok = present(j) && in_table(id);
+    if (ok) bmw = ld_u32(a.bitmask + (static_cast<uint64_t>(id) >> 5));
+    if (j >= J) return;
+    uint32_t* hb = hbuf + hs * G * scap;
+    const uint32_t per_row = a.vec ? (scap >> 2) : S;
+    const uint32_t total = G * per_row;
+    for (uint32_t t = 0; t < total; t += 32) {
+      const uint32_t c = t + lane;
+      const uint32_t q = min(c / per_row, G - 1);
+      const int64_t idq = __shfl_sync(kFull, id, q);
+      const int okq = __shfl_sync(kFull, static_cast<int>(ok), q);
+      if (c < total && okq) {
+        const uint32_t k = c - q * per_row;
+        const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
+        if (a.vec)
+          cp_async16(hb + q * scap + 4u * k, src + 4u * k);
+        else
+          cp_async4(hb + q * scap + k, src + k);
+      }
+    }
+  };
+
+  // Row kind and words to fetch, from the headers of group j (lane q).
+  auto row_info = [&](uint64_t j, uint32_t hs, int64_t id, uint32_t bmw, uint32_t& kind,
+                      uint32_t& nt) {
+    kind = kNone;
+    nt = 0;
+    if (!present(j)) return;
+    if (!in_table(id)) {
+      kind = kBadRange;
+      return;
+    }
+    if (!((bmw >> (static_cast<uint64_t>(id) & 31u)) & 1u)) {
+      kind = kRaw;
+      nt = W;
+      return;
+    }
+    const uint32_t* hb = hbuf + hs * G * scap + lane * scap;
+    uint32_t drop = 0;  // sum of popcount(Mask) over the matching words
+    for (uint32_t s = 0; s < S; ++s) {
+      const uint32_t H = hb[s];
+      if (s == S - 1) {
+        const uint32_t nb = W - 32u * s;
+        if (nb < 32u && (H >> nb)) {
+          kind = kCorrupt;
+          return;
+        }
+      }
+      if constexpr (UNIFORM) {
+        drop += __popc(H);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kPlanes; ++k) drop += __popc(H & __ldg(a.pv.planes + s * kPlanes + k)) << k;
+      }
+    }
+    if (UNIFORM) drop *= a.pv.u_p;
+    const uint32_t bits = 32u * (S + W) - drop;
+    const uint32_t Lw = (bits + 31u) >> 5;
+    if (Lw >= W) {
+      kind = kCorrupt;
+      return;
+    }
+    kind = kComp;
+    nt = Lw;
+  };
+
+  // Payload of group j -> pbuf[ps]: stream words [S, Lw) of compressed rows
+  // (from the 16-byte chunk holding word S), the whole slot of raw rows.
+  auto issue_payload = [&](uint64_t j, uint32_t ps, int64_t id, uint32_t kind, uint32_t nt) {
+    if (j >= J) return;
+    uint32_t* pb = pbuf + ps * G * rowcap;
+    for (uint32_t q = 0; q < G; ++q) {
+      const uint32_t kq = __shfl_sync(kFull, kind, q);
+      const uint32_t ntq = __shfl_sync(kFull, nt, q);
+      const int64_t idq = __shfl_sync(kFull, id, q);
+      if (kq != kRaw && kq != kComp) continue;
+      const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
+      uint32_t* dst = pb + q * rowcap;
+      if (a.vec) {
+        const uint32_t c0 = (kq == kComp) ? (S >> 2) : 0u;
+        const uint32_t c1 = (ntq + 3u) >> 2;
+        for (uint32_t c = c0 + lane; c < c1; c += 32) cp_async16(dst + 4u * c, src + 4u * c);
+      } else {
+        const uint32_t k0 = (kq == kComp) ? S : 0u;
+        for (uint32_t k = k0 + lane; k < ntq; k += 32) cp_async4(dst + k, src + k);
+      }
+    }
+  };
+
+  auto decode_group = [&](uint64_t j, uint32_t ps, uint32_t hs, uint32_t kind) {
+    const uint32_t* pbg = pbuf + ps * G * rowcap;
+    const uint32_t* hbg = hbuf + hs * G * scap;
+    const uint64_t row0 = (gw + j * nwarps) * G;
+    for (uint32_t q = 0; q < G; ++q) {
+      const uint32_t kq = __shfl_sync(kFull, kind, q);
+      if (kq == kNone) continue;
+      uint32_t* orow = a.out + (row0 + q) * W;
+      const uint32_t* pb = pbg + q * rowcap;
+      if (kq == kComp) {
+        decode_row<UNIFORM, R>(a.pv, pb, hbg + q * scap, orow, lane);
+      } else if (kq == kRaw) {
+        if (a.vec) {
+          for (uint32_t c = lane; c < (W >> 2); c += 32)
+            reinterpret_cast<uint4*>(orow)[c] = reinterpret_cast<const uint4*>(pb)[c];
+        } else {
+          for (uint32_t k = lane; k < W; k += 32) orow[k] = pb[k];
+        }
+      } else {
+        for (uint32_t k = lane; k < W; k += 32) orow[k] = 0u;
+        if (lane == 0) record_status(a.pv.status, kq == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
+      }
+    }
+  };
+
+  // Prologue: ids of groups 0..2, headers of 0 and 1, payload of 0.
+  int64_t id0 = load_id(0), id1 = load_id(1), id2 = load_id(2);
+  uint32_t bm0 = 0, bm1 = 0;
+  issue_headers(0, 0, id0, bm0);
+  cp_commit();
+  issue_headers(1, 1, id1, bm1);
+  cp_commit();
+  cp_wait<1>();
+  __syncwarp();
+  uint32_t kind0, nt0;
+  row_info(0, 0, id0, bm0, kind0, nt0);
+  issue_payload(0, 0, id0, kind0, nt0);
+  cp_commit();
+
+  // Steady state.  Stage indices: payload j in pbuf[j & 1], headers j in
+  // hbuf[j % 3] (h0 = j % 3, h1 = (j+1) % 3, h2 = (j+2) % 3).
+  uint32_t h0 = 0, h1 = 1, h2 = 2;
+  for (uint64_t j = 0; j < J; ++j) {
+    const int64_t id3 = load_id(j + 3);
+    uint32_t bm2 = 0;
+    issue_headers(j + 2, h2, id2, bm2);
+    cp_commit();
+    cp_wait<2>();  // headers of j+1 have landed
+    __syncwarp();
+    uint32_t kind1, nt1;
+    row_info(j + 1, h1, id1, bm1, kind1, nt1);
+    issue_payload(j + 1, static_cast<uint32_t>((j + 1) & 1), id1, kind1, nt1);
+    cp_commit();
+    cp_wait<2>();  // payload of j has landed
+    __syncwarp();
+    decode_group(j, static_cast<uint32_t>(j & 1), h0, kind0);
+    __syncwarp();
+    id1 = id2;
+    id2 = id3;
+    bm1 = bm2;
+    kind0 = kind1;
+    const uint32_t t = h0;
+    h0 = h1;
+    h1 = h2;
+    h2 = t;
+  }
+  cp_wait<0>();
+}
+
+template <bool U, int R>
+static int launch_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  const size_t per_warp = 4ull * (2ull * a.G * a.rowcap + 3ull * a.G * a.scap);
+  const size_t budget = 220ull * 1024;
+  size_t warps = budget / per_warp;
+  if (warps > static_cast<size_t>(kDecWarpsMax)) warps = kDecWarpsMax;
+  if (warps < 1) return IBP_EINVAL;
+  const size_t smem = warps * per_warp;
+  auto kern = k_decompress<U, R>;
+  static bool attr_set[64] = {false};
+  const int dev = plan->device;
+  if (dev < 0 || dev >= 64) return IBP_EINVAL;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) {
+      set_cuda_error(e, "cudaFuncSetAttribute(k_decompress)");
+      cudaGetLastError();
+      return IBP_ECUDA;
+    }
+    attr_set[dev] = true;
+  }
+  int occ = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, static_cast<int>(warps * 32), smem);
+  if (e != cudaSuccess || occ < 1) {
+    set_cuda_error(e, "occupancy(k_decompress)");
+    cudaGetLastError();
+    return IBP_ECUDA;
+  }
+  const uint64_t groups = (a.n_out + a.G - 1) / a.G;
+  const uint64_t need = (groups + warps - 1) / warps;
+  const uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
+  const unsigned grid = static_cast<unsigned>(need < cap ? need : cap);
+  kern<<<grid, static_cast<unsigned>(warps * 32), smem, stream>>>(a);
+  return check_launch("k_decompress");
+}
+
+int launch_decompress(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  const uint32_t runs = plan->max_runs;
+  const int R = runs <= static_cast<uint32_t>(kMaxRuns) ? (runs == 0 ? 1 : static_cast<int>(runs)) : 0;
+  if (plan->uniform) {
+    switch (R) {
+      case 1: return launch_t<true, 1>(plan, a, stream);
+      case 2: return launch_t<true, 2>(plan, a, stream);
+      case 3: return launch_t<true, 3>(plan, a, stream);
+      case 4: return launch_t<true, 4>(plan, a, stream);
+      default: return launch_t<true, 0>(plan, a, stream);
+    }
+  }
+  switch (R) {
+    case 1: return launch_t<false, 1>(plan, a, stream);
+    case 2: return launch_t<false, 2>(plan, a, stream);
+    case 3: return launch_t<false, 3>(plan, a, stream);
+    case 4: return launch_t<false, 4>(plan, a, stream);
+    default: return launch_t<false, 0>(plan, a, stream);
+  }
+}
+
+}  // namespace ibp

@@ -1,0 +1,301 @@
+"""Python binding of libibp (ctypes).  Argument marshalling only: every step
+runs in the library's CUDA kernels.  PyTorch supplies device memory, pinned
+host memory and streams.
+
+Names follow the C ABI in include/ibp.h:
+
+    mask, bitval = ibp_preprocess(sample, T)
+    plan = ibp_plan_create(mask, bitval)
+    bitmask, stored = ibp_compress(plan, rows)                 # in place
+    out = ibp_gather_decompress(plan, slots, bitmask, row_ids)
+    out = ibp_decompress_contig(plan, slots, bitmask, first_row, n)
+    ibp_get_status(plan)                                         # raises on a data error
+
+Word tensors: any contiguous tensor whose last dimension is a whole number of
+32-bit words (int32/uint32/float32, or bfloat16/float16 with an even last
+dimension) is viewed as rows of 32-bit words.  Tables passed as host tensors
+must be pinned (``pin_memory=True``): kernels read them in place (zero copy).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libibp.so")
+
+IBP_OK = 0
+IBP_EINVAL = 1
+IBP_ECUDA = 2
+IBP_ENOMEM = 3
+IBP_ECORRUPT = 4
+IBP_ERANGE = 5
+IBP_ETIMEOUT = 6
+
+_lib = None
+
+
+class IbpError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        detail = ""
+        if _lib is not None:
+            detail = _lib.ibp_last_error_detail().decode(errors="replace")
+            msg = _lib.ibp_strerror(code).decode()
+        else:
+            msg = f"status {code}"
+        super().__init__(f"{where}: {msg}" + (f" ({detail})" if detail else ""))
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_uint32), ("segments", ctypes.c_uint32), ("uniform", ctypes.c_uint32),
+                ("max_runs", ctypes.c_uint32), ("min_kept_bits", ctypes.c_uint32),
+                ("max_kept_bits", ctypes.c_uint32), ("metadata_bytes", ctypes.c_uint64),
+                ("device", ctypes.c_int)]
+
+
+def load():
+    """Load libibp.so.  Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing; build it with `python -m host_transfer_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, u64, u32, i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int
+    sigs = {
+        "ibp_strerror": ([i32], ctypes.c_char_p),
+        "ibp_version": ([], i32),
+        "ibp_last_error_detail": ([], ctypes.c_char_p),
+        "ibp_preprocess": ([vp, u64, u32, ctypes.c_double, vp, vp, vp], i32),
+        "ibp_plan_create": ([vp, vp, u32, i32, ctypes.POINTER(vp)], i32),
+        "ibp_plan_destroy": ([vp], i32),
+        "ibp_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], i32),
+        "ibp_plan_get_mask": ([vp, vp, vp], i32),
+        "ibp_compress": ([vp, vp, vp, u64, vp, vp, vp], i32),
+        "ibp_gather_decompress": ([vp, vp, u64, vp, vp, u64, vp, vp], i32),
+        "ibp_decompress_contig": ([vp, vp, u64, vp, u64, u64, vp, vp], i32),
+        "ibp_get_status": ([vp, vp], i32),
+        "ibp_gather_raw": ([vp, u64, u32, vp, u64, vp, vp], i32),
+        "ibp_row_lengths": ([vp, vp, u64, vp, vp, u64, vp, vp], i32),
+    }
+    for name, (args, res) in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(code: int, where: str):
+    if code != IBP_OK:
+        raise IbpError(code, where)
+
+
+def words(t: torch.Tensor) -> torch.Tensor:
+    """View a contiguous tensor as 32-bit words (int32), keeping its rows."""
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    if t.element_size() == 4:
+        return t.view(torch.int32)
+    if t.element_size() == 2:
+        if t.shape[-1] % 2:
+            raise ValueError("16-bit rows need an even number of elements")
+        return t.view(torch.int32)
+    if t.element_size() == 8 and t.dtype == torch.int64:
+        raise ValueError("int64 tensors are not word tensors")
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _rows(t: torch.Tensor):
+    w = words(t)
+    if w.dim() == 1:
+        w = w.view(1, -1)
+    w = w.reshape(-1, w.shape[-1])
+    return w, w.shape[0], w.shape[1]
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _device_of(*ts) -> torch.device:
+    for t in ts:
+        if t is not None and t.is_cuda:
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def ibp_preprocess(sample: torch.Tensor, T: float, mask: torch.Tensor | None = None,
+                   bitval: torch.Tensor | None = None, stream=None):
+    """Mask and Bitval (int32 device tensors of W words) from sampled rows."""
+    lib = load()
+    s, n, W = _rows(sample)
+    dev = _device_of(sample, mask, bitval)
+    if mask is None:
+        mask = torch.empty(W, dtype=torch.int32, device=dev)
+    if bitval is None:
+        bitval = torch.empty(W, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_preprocess(_ptr(s), n, W, float(T), _ptr(mask), _ptr(bitval),
+                                  _stream(stream, dev)), "ibp_preprocess")
+    return mask, bitval
+
+
+class Plan:
+    """A device plan (Mask, Bitval and derived tables).  Frees itself."""
+
+    def __init__(self, handle: int, W: int, device: int):
+        self.handle = ctypes.c_void_p(handle)
+        self.W = W
+        self.device = device
+
+    @property
+    def info(self) -> dict:
+        lib = load()
+        inf = PlanInfo()
+        _check(lib.ibp_plan_get_info(self.handle, ctypes.byref(inf)), "ibp_plan_get_info")
+        return {k: getattr(inf, k) for k, _ in PlanInfo._fields_}
+
+    def mask_bitval(self):
+        lib = load()
+        m = torch.empty(self.W, dtype=torch.int32)
+        b = torch.empty(self.W, dtype=torch.int32)
+        _check(lib.ibp_plan_get_mask(self.handle, _ptr(m), _ptr(b)), "ibp_plan_get_mask")
+        return m, b
+
+    def destroy(self):
+        if self.handle is not None and self.handle.value:
+            load().ibp_plan_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def ibp_plan_create(mask: torch.Tensor, bitval: torch.Tensor, device: int | None = None) -> Plan:
+    lib = load()
+    m = words(mask.contiguous()).reshape(-1)
+    b = words(bitval.contiguous()).reshape(-1)
+    if m.numel() != b.numel():
+        raise ValueError("mask and bitval differ in length")
+    if device is None:
+        device = m.device.index if m.is_cuda else torch.cuda.current_device()
+    h = ctypes.c_void_p()
+    _check(lib.ibp_plan_create(_ptr(m), _ptr(b), m.numel(), int(device), ctypes.byref(h)),
+           "ibp_plan_create")
+    return Plan(h.value, m.numel(), int(device))
+
+
+def bitmask_words(n_rows: int) -> int:
+    return (n_rows + 31) // 32
+
+
+def ibp_compress(plan: Plan, rows: torch.Tensor, slots: torch.Tensor | None = None,
+                 bitmask: torch.Tensor | None = None, stored: torch.Tensor | None = None,
+                 stream=None):
+    """Compress rows into slots (in place when slots is None).  Returns
+    (slots, bitmask, stored) where stored is a device int64 tensor with the
+    words a reader fetches (added to `stored` when given)."""
+    lib = load()
+    r, n, W = _rows(rows)
+    if W != plan.W:
+        raise ValueError(f"rows have {W} words, plan has {plan.W}")
+    dev = torch.device("cuda", plan.device)
+    s = r if slots is None else _rows(slots)[0]
+    if bitmask is None:
+        bitmask = torch.empty(bitmask_words(n), dtype=torch.int32, device=dev)
+    if stored is None:
+        stored = torch.zeros(1, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_compress(plan.handle, _ptr(r), _ptr(s), n, _ptr(bitmask), _ptr(stored),
+                                _stream(stream, dev)), "ibp_compress")
+    return (rows if slots is None else slots), bitmask, stored
+
+
+def ibp_gather_decompress(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor,
+                          row_ids: torch.Tensor, out: torch.Tensor | None = None, stream=None,
+                          n_rows: int | None = None) -> torch.Tensor:
+    lib = load()
+    s, n, W = _rows(slots)
+    if W != plan.W:
+        raise ValueError(f"slots have {W} words, plan has {plan.W}")
+    if row_ids.dtype != torch.int64 or not row_ids.is_contiguous():
+        raise ValueError("row_ids must be a contiguous int64 tensor")
+    dev = torch.device("cuda", plan.device)
+    k = row_ids.numel()
+    if out is None:
+        out = torch.empty((k, W), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_gather_decompress(plan.handle, _ptr(s), n if n_rows is None else n_rows,
+                                         _ptr(bitmask), _ptr(row_ids), k, _ptr(out),
+                                         _stream(stream, dev)), "ibp_gather_decompress")
+    return out
+
+
+def ibp_decompress_contig(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, first_row: int,
+                          n: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    lib = load()
+    s, n_rows, W = _rows(slots)
+    if W != plan.W:
+        raise ValueError(f"slots have {W} words, plan has {plan.W}")
+    dev = torch.device("cuda", plan.device)
+    if out is None:
+        out = torch.empty((n, W), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_decompress_contig(plan.handle, _ptr(s), n_rows, _ptr(bitmask), int(first_row),
+                                         int(n), _ptr(out), _stream(stream, dev)),
+               "ibp_decompress_contig")
+    return out
+
+
+def ibp_get_status(plan: Plan, stream=None, raise_on_error: bool = True) -> int:
+    lib = load()
+    dev = torch.device("cuda", plan.device)
+    code = lib.ibp_get_status(plan.handle, _stream(stream, dev))
+    if raise_on_error and code != IBP_OK:
+        raise IbpError(code, "ibp_get_status")
+    return code
+
+
+def ibp_row_lengths(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_ids: torch.Tensor,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Words a reader fetches per requested row (int32 device tensor)."""
+    lib = load()
+    s, n, W = _rows(slots)
+    dev = torch.device("cuda", plan.device)
+    k = row_ids.numel()
+    if out is None:
+        out = torch.empty(k, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_row_lengths(plan.handle, _ptr(s), n, _ptr(bitmask), _ptr(row_ids), k,
+                                   _ptr(out), _stream(stream, dev)), "ibp_row_lengths")
+    return out
+
+
+def ibp_gather_raw(rows: torch.Tensor, row_ids: torch.Tensor, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    lib = load()
+    r, n, W = _rows(rows)
+    dev = _device_of(row_ids, out)
+    k = row_ids.numel()
+    if out is None:
+        out = torch.empty((k, W), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_gather_raw(_ptr(r), n, W, _ptr(row_ids), k, _ptr(out), _stream(stream, dev)),
+               "ibp_gather_raw")
+    return out

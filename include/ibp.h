@@ -1,0 +1,243 @@
+/*
+ * ibp.h - C ABI of libibp, a GB300 (sm_103a) implementation of Invariant Bit
+ * Packing (IBP): lossless compression of fixed-width tensor rows by dropping
+ * the bits that a Mask marks invariant, and warp-parallel decompression of
+ * those rows from zero-copy pinned host memory or from HBM.
+ *
+ * The method is the one of "Reducing the GPU Memory Bottleneck with Lossless
+ * Compression for ML", as summarised on the page "Résumé Technique : Réduire
+ * le goulot d'étranglement de la mémoire GPU par la compression sans perte
+ * pour le ML" (sections « Algorithme central » and « Intégration au
+ * système »).  Each entry point below cites the passage it implements.
+ *
+ * ---------------------------------------------------------------------------
+ * Data format (the readings this library takes where the pages are silent)
+ * ---------------------------------------------------------------------------
+ * A row is W 32-bit words (fp32 values, or bf16/fp16 pairs with element 2j in
+ * bits 0-15).  Mask[w] marks the invariant bits of word position w and
+ * Bitval[w] their values.  Word w of a row "matches" when
+ * ((x ^ Bitval[w]) & Mask[w]) == 0; a matching word keeps its 32 - popcount(
+ * Mask[w]) non-invariant bits (in ascending order), any other word keeps all
+ * 32.  Per 32-word segment s, header word H_s has bit i set when word 32s+i
+ * matched (bits past the last word are 0).  The stream of a row is H_0 ..
+ * H_{S-1} (S = ceil(W/32)) followed by the kept fields back to back, least
+ * significant bit first (stream bit k is bit k%32 of stream word k/32).  If
+ * the stream is Lw < W words, the row's slot holds the stream and zeros after
+ * it, and the row's bit in the bitmask is 1; otherwise the slot holds the row
+ * unchanged and the bit is 0.  Bit r of the bitmask is bit r%32 of word r/32.
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions
+ * ---------------------------------------------------------------------------
+ * - Return value: an ibp_status code.  Argument errors are returned before
+ *   anything is launched.  Data errors found by a kernel (bad row id,
+ *   corrupt slot) are recorded in the plan's device status word and read by
+ *   ibp_get_status().
+ * - Memory: "device-accessible" means device memory of the plan's GPU, or
+ *   page-locked host memory mapped into the device address space (memory from
+ *   cudaHostAlloc / cudaMallocHost, or torch pin_memory=True, or memory
+ *   registered with cudaHostRegister and cudaHostRegisterMapped).  Pageable
+ *   host memory is rejected with IBP_EINVAL.  Kernels read and write mapped
+ *   host memory directly (zero copy).
+ * - Ownership: the caller owns every buffer passed in.  A plan owns its device
+ *   tables and one status word.  No call allocates on the decompress path.
+ * - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   Calls other than ibp_plan_create / ibp_plan_destroy / ibp_get_status are
+ *   asynchronous with respect to the host and ordered on `stream`.
+ * - Alignment: slots, rows and outputs whose base is 16-byte aligned and whose
+ *   W is a multiple of 4 take the 16-byte vector path; anything else takes a
+ *   4-byte path with identical results.
+ * - Limits: 1 <= W <= IBP_MAX_W words.
+ */
+#ifndef IBP_H_
+#define IBP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IBP_VERSION 1
+#define IBP_MAX_W 8192u
+
+typedef enum ibp_status {
+  IBP_OK = 0,       /* success */
+  IBP_EINVAL = 1,   /* invalid argument (size, pointer kind, T, ...) */
+  IBP_ECUDA = 2,    /* a CUDA runtime call failed; see ibp_last_error_detail() */
+  IBP_ENOMEM = 3,   /* a device allocation failed */
+  IBP_ECORRUPT = 4, /* a compressed slot announced an impossible stream */
+  IBP_ERANGE = 5,   /* a row id was outside [0, n_rows) */
+  IBP_ETIMEOUT = 6  /* a bounded wait expired */
+} ibp_status;
+
+/* Opaque per-device plan: Mask, Bitval and the derived decode tables. */
+typedef struct ibp_plan ibp_plan;
+
+typedef struct ibp_plan_info {
+  uint32_t W;              /* words per row */
+  uint32_t segments;       /* ceil(W / 32): header words per compressed row */
+  uint32_t uniform;        /* 1 when every word position has the same Mask and Bitval */
+  uint32_t max_runs;       /* most runs of kept (non-invariant) bits in one word */
+  uint32_t min_kept_bits;  /* fewest kept bits of any word position */
+  uint32_t max_kept_bits;  /* most kept bits of any word position */
+  uint64_t metadata_bytes; /* device bytes of the plan's tables (Mask + Bitval + derived) */
+  int device;              /* CUDA device of the plan */
+} ibp_plan_info;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* ibp_strerror(int status);
+
+/* IBP_VERSION of the loaded library. */
+int ibp_version(void);
+
+/* Text of the last CUDA error seen by a library call on this thread ("" if
+ * none).  Valid until the next library call on this thread. */
+const char* ibp_last_error_detail(void);
+
+/*
+ * Preprocess - « Algorithme central », step 1 (Prétraitement): analyse a batch
+ * of rows and find the bit positions that hold the same value in at least a
+ * fraction T of them; emit a fixed-size Mask (which positions) and Bitval
+ * (their values).
+ *
+ * sample  device-accessible, s_rows x W words, row-major.
+ * s_rows  number of sampled rows, 1 <= s_rows < 2^32.
+ * W       words per row, 1 <= W <= IBP_MAX_W.
+ * T       fraction in (0, 1].  With t = ceil(T * s_rows) evaluated in IEEE
+ *         double, bit b of word w is invariant when max(#ones, #zeros) >= t
+ *         over the sample; its Bitval bit is 1 when #ones > #zeros (a tie
+ *         gives 0).  Bitval is 0 outside the Mask.
+ * mask, bitval  device-accessible outputs of W words each.
+ * stream  CUDA stream; the results are ready when the stream reaches them.
+ *
+ * Uses 128 * W bytes of device scratch, allocated and freed in stream order
+ * (cudaMallocAsync / cudaFreeAsync).  Errors: IBP_EINVAL (sizes, T, pointer
+ * kinds), IBP_ENOMEM, IBP_ECUDA.
+ */
+int ibp_preprocess(const uint32_t* sample, uint64_t s_rows, uint32_t W, double T,
+                   uint32_t* mask, uint32_t* bitval, void* stream);
+
+/*
+ * Plan - « Algorithme central », step 1, last point: the Mask/Bitval metadata
+ * is kept in GPU memory (a few kilobytes) and reused for the whole dataset.
+ * Copies Mask and Bitval to `device` and derives the per-word decode tables
+ * there (kept-bit counts, runs of kept bits, shift tables).
+ *
+ * mask, bitval  W words each, in any memory (pageable host, pinned host or
+ *               device); read once during the call.  Bitval bits outside the
+ *               Mask are ignored.
+ * device        CUDA device ordinal that will run the plan's kernels.
+ * out           receives the new plan; unchanged on error.
+ *
+ * Synchronous.  Errors: IBP_EINVAL, IBP_ENOMEM, IBP_ECUDA.
+ */
+int ibp_plan_create(const uint32_t* mask, const uint32_t* bitval, uint32_t W, int device,
+                    ibp_plan** out);
+
+/* Frees the plan's device memory (synchronises its device).  NULL is ignored. */
+int ibp_plan_destroy(ibp_plan* plan);
+
+/* Fills *out with the plan's shape and table statistics. */
+int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out);
+
+/* The plan's Mask and Bitval (W words each) copied to host memory `mask` and
+ * `bitval` (either may be NULL).  Synchronous. */
+int ibp_plan_get_mask(const ibp_plan* plan, uint32_t* mask, uint32_t* bitval);
+
+/*
+ * Compress - « Algorithme central », step 2 (Compression), run on the GPU over
+ * zero-copy memory, and « Intégration au système » (fixed-size in-place
+ * buffers, a GPU-resident bitmask of the compressed tensors).  One warp per
+ * row: match test per word, removal of the invariant bits, participation
+ * headers by warp ballot, bit offsets by warp scan, row kept raw when the
+ * stream would not be shorter than the row.
+ *
+ * rows          device-accessible input, n_rows x W words.
+ * slots         device-accessible output, n_rows x W words.  May be the same
+ *               pointer as rows (in-place); must not overlap it otherwise.
+ * n_rows        rows to compress (0 is a no-op).
+ * bitmask       device-accessible output of ceil(n_rows / 32) words, fully
+ *               written (bits past n_rows are 0).
+ * stored_words  optional device-accessible uint64: the number of words a
+ *               reader fetches for these rows (Lw per compressed row, W per raw
+ *               row) is ADDED to it.  NULL to skip.
+ *
+ * Asynchronous on `stream`.  Errors: IBP_EINVAL, IBP_ECUDA.
+ */
+int ibp_compress(const ibp_plan* plan, const uint32_t* rows, uint32_t* slots, uint64_t n_rows,
+                 uint32_t* bitmask, uint64_t* stored_words, void* stream);
+
+/*
+ * Gather-decompress - « Algorithme central », step 3 (Décompression): a warp
+ * reads a row's compressed segment from CPU (or GPU) memory into a shared-
+ * memory workspace, computes each lane's starting bit offset with warp
+ * primitives, rebuilds its words by reinserting the Bitval bits at the Mask
+ * positions, and overlaps the fetch of the next rows with the decoding of the
+ * current ones.  Only the compressed prefix of a slot is read.
+ *
+ * slots    device-accessible, the whole table: n_rows x W words (the output
+ *          of ibp_compress, or the same format from any writer).
+ * n_rows   rows in the table; ids must lie in [0, n_rows).
+ * bitmask  device-accessible, ceil(n_rows / 32) words.
+ * row_ids  device-accessible, n_ids int64 row ids (repeats allowed).
+ * out      device-accessible, n_ids x W words: out row i = row row_ids[i].
+ *
+ * An id outside [0, n_rows) records IBP_ERANGE and gives a zero row; a
+ * compressed slot whose headers announce a stream of W words or more, or set
+ * a header bit past the last word, records IBP_ECORRUPT and gives a zero row.
+ * Asynchronous on `stream`; no allocation.  Errors: IBP_EINVAL, IBP_ECUDA.
+ */
+int ibp_gather_decompress(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                          const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
+                          uint32_t* out, void* stream);
+
+/*
+ * Contiguous decompress - step 3 for the rows first_row .. first_row + n - 1
+ * of the table (e.g. one offloaded weight matrix or KV block), written to a
+ * dense n x W output.  Arguments as for ibp_gather_decompress; first_row + n
+ * must not exceed n_rows (IBP_EINVAL).
+ */
+int ibp_decompress_contig(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                          const uint32_t* bitmask, uint64_t first_row, uint64_t n,
+                          uint32_t* out, void* stream);
+
+/*
+ * Synchronises `stream`, returns the first data error recorded by the plan's
+ * kernels since the last call (IBP_OK if none) and clears it.  The status
+ * word is shared by every call made with this plan, on any stream.
+ */
+int ibp_get_status(const ibp_plan* plan, void* stream);
+
+/*
+ * Fetched length per row - « Intégration au système »: a fixed-size buffer of
+ * which only the compressed part is read.  lengths[i] = words a reader
+ * fetches for row row_ids[i]: Lw (the stream length announced by the row's
+ * headers) for a compressed row, W for a raw row, 0 for an id outside
+ * [0, n_rows) (which also records IBP_ERANGE).  A compressed row whose headers
+ * announce W words or more reports W.
+ *
+ * slots, bitmask, row_ids  as for ibp_gather_decompress.
+ * lengths  device-accessible output, n_ids uint32.
+ * Asynchronous on `stream`.  Errors: IBP_EINVAL, IBP_ECUDA.
+ */
+int ibp_row_lengths(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                    const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
+                    uint32_t* lengths, void* stream);
+
+/*
+ * Uncompressed gather (measurement baseline): out row i = rows row
+ * row_ids[i], the ideal uncompressed transfer of the same rows that
+ * ibp_gather_decompress rebuilds (« Résultats », overhead against the ideal
+ * uncompressed transfer rate).  Ids outside [0, n_rows) give zero rows.
+ * Arguments as for ibp_gather_decompress.  Asynchronous on `stream`.
+ */
+int ibp_gather_raw(const uint32_t* rows, uint64_t n_rows, uint32_t W, const int64_t* row_ids,
+                   uint64_t n_ids, uint32_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IBP_H_ */

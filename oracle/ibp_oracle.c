@@ -61,21 +61,27 @@ int ibp_ref_preprocess(const uint32_t* sample, uint64_t s_rows, uint32_t W,
                        double T, uint32_t* mask, uint32_t* bitval) {
   if (s_rows == 0 || W == 0 || !(T > 0.0 && T <= 1.0)) return REF_EINVAL;
   uint64_t t = (uint64_t)ceil(T * (double)s_rows);
+  /* ones[w*32 + b] = number of sampled rows with bit b of word w set; the
+   * rows are read once, in order */
+  uint64_t* ones = (uint64_t*)calloc((size_t)W * 32, sizeof(uint64_t));
+  for (uint64_t r = 0; r < s_rows; ++r)
+    for (uint32_t w = 0; w < W; ++w)
+      for (unsigned b = 0; b < 32; ++b) ones[w * 32 + b] += bit_of(sample[r * W + w], b);
   for (uint32_t w = 0; w < W; ++w) {
     uint32_t m = 0, v = 0;
     for (unsigned b = 0; b < 32; ++b) {
-      uint64_t ones = 0;
-      for (uint64_t r = 0; r < s_rows; ++r) ones += bit_of(sample[r * W + w], b);
-      uint64_t zeros = s_rows - ones;
-      uint64_t most = ones > zeros ? ones : zeros;
+      uint64_t n1 = ones[w * 32 + b];
+      uint64_t n0 = s_rows - n1;
+      uint64_t most = n1 > n0 ? n1 : n0;
       if (most >= t) {
         m |= 1u << b;
-        if (ones > zeros) v |= 1u << b;
+        if (n1 > n0) v |= 1u << b;
       }
     }
     mask[w] = m;
     bitval[w] = v;
   }
+  free(ones);
   return REF_OK;
 }
 

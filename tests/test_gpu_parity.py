@@ -1,0 +1,341 @@
+"""Bit-exact parity of the CUDA path with the CPU oracle.
+
+Small cases are compared whole (Mask/Bitval, every slot word, the bitmask,
+the stored-word count, every decoded word); they span several warps and
+groups, ragged segments and ragged row counts.  Edge cases: empty calls,
+one-word rows, widths that are not multiples of 4 or 32 (the 4-byte path),
+unaligned buffers, masks of 0 and of all ones, random masks (five-step
+expand path), per-word masks (table path), special floats, repeated and
+out-of-range ids, corrupt slots.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from host_transfer_gb300 import ibp, workloads
+from oracle import oracle_c as C
+from tests.gpu_util import empty_like_in, gpu_codec, on_device, pinned, place, words_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from host_transfer_gb300 import build
+
+    build.build()
+    ibp.load()
+    C.set_threads(8)
+
+
+def _check_codec(rows, sample, T, where, inplace=False):
+    """Full comparison of preprocess + compress + decompress with the oracle."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint32)
+    g = gpu_codec(rows, sample, T, where, inplace)
+    st, m, b = C.preprocess(sample, T)
+    assert st == 0
+    assert np.array_equal(g["mask"], m), "Mask differs from the oracle"
+    assert np.array_equal(g["bitval"], b), "Bitval differs from the oracle"
+    slots, bitmask, stored = C.compress(rows, m, b)
+    assert np.array_equal(words_np(g["slots_t"]), slots), "slots differ from the oracle"
+    assert np.array_equal(g["bitmask"], bitmask), "bitmask differs from the oracle"
+    assert g["stored"] == stored
+    # gather every row in a shuffled order with repeats
+    n = rows.shape[0]
+    rng = np.random.default_rng(n)
+    ids = np.concatenate([rng.permutation(n), rng.integers(0, n, n // 3 + 1)]).astype(np.int64)
+    ids_t = torch.from_numpy(ids).cuda()
+    bm_t = on_device(g["bitmask"])
+    out = ibp.ibp_gather_decompress(g["plan"], g["slots_t"], bm_t, ids_t)
+    torch.cuda.synchronize()
+    assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
+    assert np.array_equal(words_np(out), rows[ids])
+    return g, ids
+
+
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_tiny_config_full_parity(where):
+    c = workloads.CONFIGS["tiny"]
+    rows = workloads.make_table("tiny")
+    sample = rows[workloads.sample_ids(c["n_rows"], c["sample"], c["sample_seed"])]
+    g, _ = _check_codec(rows, sample, c["T"], where)
+    # contiguous decompress of a ragged middle range
+    bm_t = on_device(g["bitmask"])
+    out = ibp.ibp_decompress_contig(g["plan"], g["slots_t"], bm_t, 37, 1500)
+    torch.cuda.synchronize()
+    assert np.array_equal(words_np(out), rows[37:1537])
+    info = g["plan"].info
+    assert info["W"] == 128 and info["segments"] == 4
+
+
+def test_tiny_config_in_place_compress():
+    c = workloads.CONFIGS["tiny"]
+    rows = workloads.make_table("tiny")
+    sample = rows[workloads.sample_ids(c["n_rows"], c["sample"], c["sample_seed"])]
+    g = gpu_codec(rows, sample, c["T"], "host", inplace=True)
+    slots, bitmask, stored = C.compress(rows, g["mask"], g["bitval"])
+    assert np.array_equal(words_np(g["slots_t"]), slots)
+    assert np.array_equal(g["bitmask"], bitmask)
+
+
+def _float_rows(rng, n, W, scale=0.05):
+    return rng.normal(0, scale, (n, W)).astype(np.float32).view(np.uint32)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 8, 31, 32, 33, 63, 64, 100, 127, 128, 129, 255, 256,
+                               257, 512, 1000, 1024, 2048, 4096, 8192])
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_widths_learned_masks(W, where):
+    rng = np.random.default_rng(W)
+    n = max(33, min(700, 200_000 // W))
+    rows = _float_rows(rng, n, W)
+    rows[::9] = rng.integers(0, 2**32, (len(rows[::9]), W), dtype=np.uint64).astype(np.uint32)
+    _check_codec(rows, rows[: max(1, n // 2)], 0.9, where)
+
+
+@pytest.mark.parametrize("W", [4, 33, 128, 300])
+def test_per_word_masks_table_path(W):
+    """Columns with different scales give different Masks per word position."""
+    rng = np.random.default_rng(100 + W)
+    scale = np.exp(rng.uniform(-8, 3, W))
+    x = (rng.normal(0, 1, (400, W)) * scale).astype(np.float32)
+    x[:, ::3] = np.abs(x[:, ::3])
+    rows = x.view(np.uint32)
+    g, _ = _check_codec(rows, rows[:300], 0.97, "hbm")
+    assert g["plan"].info["uniform"] == 0
+
+
+@pytest.mark.parametrize("W", [7, 64, 160])
+@pytest.mark.parametrize("runs", ["many", "few"])
+def test_random_masks(W, runs):
+    """Arbitrary Mask/Bitval (up to 16 runs of kept bits: five-step path)."""
+    rng = np.random.default_rng(W)
+    n = 300
+    if runs == "many":
+        base = rng.integers(0, 2**32, W, dtype=np.uint64).astype(np.uint32)
+    else:
+        base = np.full(W, 0x3F800000, np.uint32)
+    rows = rng.integers(0, 2**32, (n, W), dtype=np.uint64).astype(np.uint32)
+    keepers = rng.integers(0, 2**32, W, dtype=np.uint64).astype(np.uint32)
+    if runs == "few":
+        keepers = np.full(W, 0x807F00FF, np.uint32)
+    # most rows agree with base outside `keepers`
+    agree = rng.random(n) < 0.8
+    rows[agree] = (rows[agree] & keepers) | (base & ~keepers)
+    g, _ = _check_codec(rows, rows[:200], 0.75, "hbm")
+    if runs == "many":
+        assert g["plan"].info["max_runs"] > 4
+
+
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_mask_zero_all_raw(where):
+    """Sample rows that agree on nothing leave the Mask empty: every row raw."""
+    W = 64
+    rows = np.random.default_rng(1).integers(0, 2**32, (100, W), dtype=np.uint64).astype(np.uint32)
+    sample = np.stack([np.zeros(W, np.uint32), np.full(W, 0xFFFFFFFF, np.uint32)])
+    g, _ = _check_codec(rows, sample, 1.0, where)
+    assert not g["bitmask"].any() and g["plan"].info["max_kept_bits"] == 32
+
+
+@pytest.mark.parametrize("W", [1, 6, 32, 33, 200])
+def test_full_mask_headers_only(W):
+    bv = (np.arange(W, dtype=np.uint64) * 2654435761 % 2**32).astype(np.uint32)
+    rows = np.tile(bv, (70, 1))
+    rows[5, 0] ^= 1  # one row breaks one word
+    g, _ = _check_codec(rows, np.tile(bv, (3, 1)), 1.0, "hbm")
+    S = (W + 31) // 32
+    if W > 1:
+        assert g["stored"] == 69 * S + min(W, S + 1)
+
+
+def test_special_floats_round_trip():
+    rng = np.random.default_rng(5)
+    W = 96
+    vals = np.array([np.nan, np.inf, -np.inf, -0.0, 0.0, 1e-45, -1e-40, 3.4e38, 1.0, -2.5],
+                    np.float32).view(np.uint32)
+    rows = _float_rows(rng, 500, W)
+    rows[::7, ::5] = vals[rng.integers(0, len(vals), rows[::7, ::5].shape)]
+    rows[3, :] = vals[rng.integers(0, len(vals), W)]
+    _check_codec(rows, rows, 0.95, "host")
+
+
+def test_bf16_pairs_round_trip():
+    rng = np.random.default_rng(6)
+    x = rng.normal(0, 0.02, (300, 256)).astype(np.float32)
+    rows = workloads.bf16_pairs_to_words(workloads.f32_to_bf16_bits(x))
+    _check_codec(rows, rows[:128], 0.99, "host")
+
+
+def test_unaligned_buffers_take_the_word_path():
+    """Slots and outputs offset by one word are not 16-byte aligned."""
+    rng = np.random.default_rng(7)
+    W, n = 128, 300
+    rows = _float_rows(rng, n, W)
+    s = on_device(rows[:200])
+    mask, bitval = ibp.ibp_preprocess(s, 0.95)
+    plan = ibp.ibp_plan_create(mask, bitval)
+    buf = torch.empty(n * W + 1, dtype=torch.int32, pin_memory=True)
+    buf[1:].numpy()[...] = rows.reshape(-1).view(np.int32)
+    rows_t = buf[1:].view(n, W)
+    sbuf = torch.empty(n * W + 1, dtype=torch.int32, pin_memory=True)
+    slots_t = sbuf[1:].view(n, W)
+    _, bitmask, stored = ibp.ibp_compress(plan, rows_t, slots_t)
+    obuf = torch.empty(n * W + 1, dtype=torch.int32, device="cuda")
+    out = obuf[1:].view(n, W)
+    ids = torch.arange(n - 1, -1, -1, dtype=torch.int64, device="cuda")
+    ibp.ibp_gather_decompress(plan, slots_t, bitmask, ids, out=out)
+    torch.cuda.synchronize()
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+    ms, mb = words_np(mask), words_np(bitval)
+    cs, cb, _ = C.compress(rows, ms, mb)
+    assert np.array_equal(words_np(slots_t), cs) and np.array_equal(words_np(bitmask), cb)
+    assert np.array_equal(words_np(out), rows[::-1])
+
+
+def test_decoder_on_oracle_slots():
+    """The decoder alone, on slots the oracle wrote."""
+    rng = np.random.default_rng(8)
+    for W in (16, 128, 129, 600):
+        rows = _float_rows(rng, 257, W, scale=1e-3)
+        _, m, b = C.preprocess(rows[:100], 0.99)
+        slots, bitmask, _ = C.compress(rows, m, b)
+        plan = ibp.ibp_plan_create(torch.from_numpy(m.view(np.int32)), torch.from_numpy(b.view(np.int32)))
+        for where in ("host", "hbm"):
+            st = place(slots, where)
+            ids = torch.from_numpy(rng.integers(0, 257, 999)).cuda()
+            out = ibp.ibp_gather_decompress(plan, st, on_device(bitmask), ids)
+            torch.cuda.synchronize()
+            assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+            assert np.array_equal(words_np(out), rows[ids.cpu().numpy()])
+
+
+def test_empty_calls_are_no_ops():
+    rows = np.zeros((4, 8), np.uint32)
+    g = gpu_codec(rows, rows, 0.9, "hbm")
+    plan = g["plan"]
+    empty_ids = torch.empty(0, dtype=torch.int64, device="cuda")
+    out = ibp.ibp_gather_decompress(plan, g["slots_t"], on_device(g["bitmask"]), empty_ids)
+    assert out.shape == (0, 8)
+    out = ibp.ibp_decompress_contig(plan, g["slots_t"], on_device(g["bitmask"]), 0, 0)
+    assert out.shape == (0, 8)
+    _, bm, st = ibp.ibp_compress(plan, torch.empty((0, 8), dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+
+
+def test_out_of_range_ids_give_zero_rows_and_erange():
+    c = workloads.CONFIGS["tiny"]
+    rows = workloads.make_table("tiny")
+    g = gpu_codec(rows, rows[:256], c["T"], "hbm")
+    n = rows.shape[0]
+    ids = np.array([0, n, -1, 5, 2**40, n - 1, -(2**62)], np.int64)
+    out = ibp.ibp_gather_decompress(g["plan"], g["slots_t"], on_device(g["bitmask"]),
+                                    torch.from_numpy(ids).cuda())
+    code = ibp.ibp_get_status(g["plan"], raise_on_error=False)
+    assert code == ibp.IBP_ERANGE
+    o = words_np(out)
+    assert np.array_equal(o[[0, 3, 5]], rows[[0, 5, n - 1]])
+    assert not o[[1, 2, 4, 6]].any()
+    st, ref = C.decompress(words_np(g["slots_t"]), g["bitmask"], ids, g["mask"], g["bitval"])
+    assert st == ibp.IBP_ERANGE and np.array_equal(o, ref)
+    # the status was cleared by the read
+    assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
+
+
+@pytest.mark.parametrize("W", [40, 128])
+def test_corrupt_slots_give_zero_rows_and_ecorrupt(W):
+    rng = np.random.default_rng(9)
+    rows = _float_rows(rng, 64, W)
+    g = gpu_codec(rows, rows, 0.9, "host")
+    assert g["bitmask"][0] & 0b111 == 0b111
+    slots = words_np(g["slots_t"]).copy()
+    S = (W + 31) // 32
+    slots[0, :S] = 0  # every word announces 32 bits: stream >= W words
+    if W % 32:
+        slots[1, S - 1] |= 1 << 31  # header bit past the last word
+    bad = pinned(slots)
+    ids = np.arange(4, dtype=np.int64)
+    out = ibp.ibp_gather_decompress(g["plan"], bad, on_device(g["bitmask"]), torch.from_numpy(ids).cuda())
+    code = ibp.ibp_get_status(g["plan"], raise_on_error=False)
+    assert code == ibp.IBP_ECORRUPT
+    o = words_np(out)
+    st, ref = C.decompress(slots, g["bitmask"], ids, g["mask"], g["bitval"])
+    assert st == ibp.IBP_ECORRUPT and np.array_equal(o, ref)
+    assert not o[0].any() and np.array_equal(o[2:], rows[2:4])
+
+
+def test_preprocess_edge_cases():
+    rng = np.random.default_rng(10)
+    cases = [
+        (rng.integers(0, 2**32, (1, 37), dtype=np.uint64).astype(np.uint32), 1.0),
+        (np.array([[0x0F0F0F0F, 1], [0xF0F0F0F0, 1]], np.uint32), 0.5),
+        (np.array([[1], [1], [1], [0]], np.uint32), 0.75),
+        (np.array([[1], [1], [1], [0]], np.uint32), 0.76),
+        (rng.integers(0, 2**32, (4097, 33), dtype=np.uint64).astype(np.uint32), 0.5),
+        (_float_rows(rng, 5000, 1000), 0.999),
+    ]
+    for sample, T in cases:
+        for where in ("host", "hbm"):
+            s = place(sample, where)
+            m, b = ibp.ibp_preprocess(s, T)
+            torch.cuda.synchronize()
+            st, rm, rb = C.preprocess(sample, T)
+            assert np.array_equal(words_np(m), rm) and np.array_equal(words_np(b), rb)
+
+
+def test_preprocess_rejects_bad_arguments():
+    s = torch.zeros((4, 4), dtype=torch.int32, device="cuda")
+    for T in (0.0, -1.0, 1.5, float("nan")):
+        with pytest.raises(ibp.IbpError):
+            ibp.ibp_preprocess(s, T)
+    pageable = torch.zeros((4, 4), dtype=torch.int32)
+    with pytest.raises(ibp.IbpError):
+        ibp.ibp_preprocess(pageable, 0.9)
+
+
+def test_gather_raw_matches_rows():
+    rng = np.random.default_rng(11)
+    for W in (3, 64, 128):
+        rows = rng.integers(0, 2**32, (1000, W), dtype=np.uint64).astype(np.uint32)
+        ids = rng.integers(-5, 1005, 3000).astype(np.int64)
+        for where in ("host", "hbm"):
+            out = ibp.ibp_gather_raw(place(rows, where), torch.from_numpy(ids).cuda())
+            torch.cuda.synchronize()
+            want = np.where(((ids >= 0) & (ids < 1000))[:, None], rows[np.clip(ids, 0, 999)], 0)
+            assert np.array_equal(words_np(out), want)
+
+
+def test_streams_and_repeated_calls_agree():
+    """Two plans on two streams, calls repeated: identical results."""
+    c = workloads.CONFIGS["tiny"]
+    rows = workloads.make_table("tiny")
+    g = gpu_codec(rows, rows[:256], c["T"], "host")
+    bm_t = on_device(g["bitmask"])
+    ids = torch.from_numpy(np.random.default_rng(3).integers(0, 2048, 4096)).cuda()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for s in (s1, s2, s1):
+        with torch.cuda.stream(s):
+            outs.append(ibp.ibp_gather_decompress(g["plan"], g["slots_t"], bm_t, ids, stream=s))
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, outs[0])
+    assert np.array_equal(words_np(outs[0]), rows[ids.cpu().numpy()])
+
+
+@pytest.mark.parametrize("W", [5, 64, 128, 300])
+def test_row_lengths_match_oracle_stored_words(W):
+    rng = np.random.default_rng(12 + W)
+    rows = _float_rows(rng, 200, W)
+    rows[::11] = rng.integers(0, 2**32, (len(rows[::11]), W), dtype=np.uint64).astype(np.uint32)
+    g = gpu_codec(rows, rows[:100], 0.9, "host")
+    ids = np.concatenate([np.arange(200), [-1, 200, 7]]).astype(np.int64)
+    lens = ibp.ibp_row_lengths(g["plan"], g["slots_t"], on_device(g["bitmask"]),
+                               torch.from_numpy(ids).cuda())
+    code = ibp.ibp_get_status(g["plan"], raise_on_error=False)
+    assert code == ibp.IBP_ERANGE
+    want = [C.compress(rows[i:i + 1], g["mask"], g["bitval"])[2] for i in range(200)]
+    got = lens.cpu().numpy()
+    assert got[:200].tolist() == want
+    assert got[200] == 0 and got[201] == 0 and got[202] == want[7]
