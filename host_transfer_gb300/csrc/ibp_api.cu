@@ -17,6 +17,8 @@ void set_cuda_error(cudaError_t e, const char* where) {
   snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
 }
 
+void clear_error_detail() { g_detail[0] = 0; }
+
 int check_launch(const char* where) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -70,6 +70,7 @@ namespace ibp {
 // Host-side helpers (ibp_api.cu)
 
 void set_cuda_error(cudaError_t e, const char* where);
+void clear_error_detail();
 int check_launch(const char* where);
 // Resolves a pointer to an address a kernel on `device` can dereference.
 // Accepts device memory of `device`, managed memory, and mapped pinned host
@@ -112,6 +113,12 @@ int launch_compress(const ibp_plan* plan, CompressArgs& a, cudaStream_t stream);
 
 int launch_preprocess(const uint32_t* sample, uint64_t s_rows, uint32_t W, double T,
                       uint32_t* mask, uint32_t* bitval, cudaStream_t stream);
+
+// The two preprocess launches (bit counts, then Mask/Bitval) on a caller-
+// provided zeroed counter array of 32 * W words.
+int launch_count_and_threshold(const uint32_t* sample, uint64_t s_rows, uint32_t W, double T,
+                               uint32_t* ones, uint32_t* mask, uint32_t* bitval,
+                               cudaStream_t stream);
 
 // Builds the tables of a plan whose d_block is allocated and whose mask and
 // bitval arrays already hold the caller's Mask/Bitval.  Fills the summary

@@ -98,6 +98,20 @@ int launch_preprocess(const uint32_t* sample, uint64_t s_rows, uint32_t W, doubl
   return rc;
 }
 
+int launch_count_and_threshold(const uint32_t* sample, uint64_t s_rows, uint32_t W, double T,
+                               uint32_t* ones, uint32_t* mask, uint32_t* bitval,
+                               cudaStream_t stream) {
+  uint64_t per_block = kRowsPerCountBlock;
+  if ((s_rows + per_block - 1) / per_block > 65535) per_block = (s_rows + 65534) / 65535;
+  const uint64_t yblocks = (s_rows + per_block - 1) / per_block;
+  dim3 grid((W + kCountThreads - 1) / kCountThreads, static_cast<unsigned>(yblocks));
+  k_count_ones<<<grid, kCountThreads, 0, stream>>>(sample, s_rows, W, per_block, ones);
+  int rc = check_launch("k_count_ones");
+  if (rc != IBP_OK) return rc;
+  k_mask_from_counts<<<(W + 127) / 128, 128, 0, stream>>>(ones, s_rows, W, T, mask, bitval);
+  return check_launch("k_mask_from_counts");
+}
+
 // ---------------------------------------------------------------------------
 // Plan tables
 

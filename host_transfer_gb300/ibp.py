@@ -71,6 +71,7 @@ def load():
         "ibp_version": ([], i32),
         "ibp_last_error_detail": ([], ctypes.c_char_p),
         "ibp_preprocess": ([vp, u64, u32, ctypes.c_double, vp, vp, vp], i32),
+        "ibp_preprocess_noalloc": ([vp, u64, u32, ctypes.c_double, vp, vp, vp], i32),
         "ibp_plan_create": ([vp, vp, u32, i32, ctypes.POINTER(vp)], i32),
         "ibp_plan_destroy": ([vp], i32),
         "ibp_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], i32),
@@ -150,6 +151,20 @@ def ibp_preprocess(sample: torch.Tensor, T: float, mask: torch.Tensor | None = N
     with torch.cuda.device(dev):
         _check(lib.ibp_preprocess(_ptr(s), n, W, float(T), _ptr(mask), _ptr(bitval),
                                   _stream(stream, dev)), "ibp_preprocess")
+    return mask, bitval
+
+
+def ibp_preprocess_noalloc(sample: torch.Tensor, T: float, mask: torch.Tensor, bitval: torch.Tensor,
+                           stream=None):
+    """ibp_preprocess for callers that cannot let the library allocate device
+    memory: its scratch is a fixed per-GPU array (W <= IBP_NOALLOC_MAX_W), and
+    the caller passes the outputs.  Calls that overlap on the GPU race."""
+    lib = load()
+    s, n, W = _rows(sample)
+    dev = _device_of(sample, mask, bitval)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_preprocess_noalloc(_ptr(s), n, W, float(T), _ptr(mask), _ptr(bitval),
+                                          _stream(stream, dev)), "ibp_preprocess_noalloc")
     return mask, bitval
 
 

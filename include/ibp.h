@@ -61,6 +61,7 @@ extern "C" {
 
 #define IBP_VERSION 1
 #define IBP_MAX_W 8192u
+#define IBP_NOALLOC_MAX_W 4096u
 
 typedef enum ibp_status {
   IBP_OK = 0,       /* success */
@@ -118,6 +119,34 @@ const char* ibp_last_error_detail(void);
  */
 int ibp_preprocess(const uint32_t* sample, uint64_t s_rows, uint32_t W, double T,
                    uint32_t* mask, uint32_t* bitval, void* stream);
+
+/*
+ * Preprocess that allocates nothing.  The paper has no counterpart: this
+ * entry point exists for callers that cannot let a library allocate device
+ * memory - a process whose device memory is wholly owned by its own allocator
+ * (a framework's caching allocator, an arena reserved at start-up), or a
+ * device or driver without stream-ordered memory pools
+ * (cudaDevAttrMemoryPoolsSupported = 0), where the cudaMallocAsync scratch of
+ * ibp_preprocess is not an option.
+ *
+ * Same arguments, results and errors as ibp_preprocess, on the current
+ * device.  The per-bit counters live instead in a fixed array of
+ * IBP_NOALLOC_MAX_W * 32 words (512 KiB) that the library places in the
+ * memory of every GPU it is loaded on, held until the process exits.  No
+ * cudaMalloc, cudaFree or other allocating call is made.
+ *
+ * - W must be at most IBP_NOALLOC_MAX_W; a larger W returns IBP_EINVAL before
+ *   anything runs.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ * - Every call on a device shares the one array, and each call clears the part
+ *   it uses on `stream` before counting: calls that overlap on the GPU (on
+ *   different streams, without ordering between them) race and give wrong
+ *   Masks.  Order such calls on one stream or with events.
+ */
+int ibp_preprocess_noalloc(const uint32_t* sample, uint64_t s_rows, uint32_t W, double T,
+                           uint32_t* mask, uint32_t* bitval, void* stream);
 
 /*
  * Plan - « Algorithme central », step 1, last point: the Mask/Bitval metadata
