@@ -398,12 +398,14 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     ibp.ibp_get_status(plan)
     g0, g1 = ev(), ev()
+    torch.cuda.nvtx.range_push("host_timed")  # ncu --nvtx --nvtx-include host_timed/
     g0.record(stream)
     for k in range(K):
         starts[k].record(stream)
         ibp.ibp_gather_decompress(plan, table, bitmask, ids_d[(WU + k) % pool], out=out)
         ends[k].record(stream)
     g1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
@@ -418,12 +420,14 @@ def run_ours(args):
     hs = [ev() for _ in range(K)]
     he = [ev() for _ in range(K)]
     a, b = ev(), ev()
+    torch.cuda.nvtx.range_push("hbm_timed")  # ncu --nvtx --nvtx-include hbm_timed/
     a.record(stream)
     for k in range(K):
         hs[k].record(stream)
         ibp.ibp_gather_decompress(plan, table_d, bitmask, ids_d[(WU + k) % pool], out=out)
         he[k].record(stream)
     b.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     hbm_total_ms = a.elapsed_time(b)
     hbm_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(hs, he))

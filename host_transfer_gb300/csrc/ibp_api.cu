@@ -263,7 +263,7 @@ int ibp_compress(const ibp_plan* plan, const uint32_t* rows, uint32_t* slots, ui
   a.bitmask = const_cast<uint32_t*>(static_cast<const uint32_t*>(db));
   a.stored = const_cast<unsigned long long*>(static_cast<const unsigned long long*>(dst));
   a.vec = (W % 4 == 0) && aligned16(a.rows) && aligned16(a.slots);
-  a.rowcap = static_cast<uint32_t>(((W + 3) / 4) * 4 + 4);
+  a.rowcap = static_cast<uint32_t>(((W + 31) / 32) * 32);
   return launch_compress(plan, a, static_cast<cudaStream_t>(stream));
 }
 
@@ -289,9 +289,12 @@ static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64
   a.n_out = n_out;
   a.out = const_cast<uint32_t*>(static_cast<const uint32_t*>(dout));
   a.vec = (W % 4 == 0) && aligned16(a.slots) && aligned16(a.out);
-  a.rowcap = static_cast<uint32_t>(((W + 3) / 4) * 4 + 4);
-  a.scap = ((plan->S + 3) / 4) * 4;
-  uint32_t G = 1152u / a.rowcap;
+  a.rowcap = static_cast<uint32_t>(((W + 31) / 32) * 32);
+  // prefix: the shortest possible stream, in whole 16-byte chunks on the
+  // vector path (never past the row: W % 4 == 0 there)
+  a.pre = a.vec ? ((plan->lmin + 3u) / 4u) * 4u : plan->lmin;
+  if (a.pre > W) a.pre = static_cast<uint32_t>(W);
+  uint32_t G = 1152u / static_cast<uint32_t>(W + 4);
   a.G = G < 1 ? 1 : (G > 32 ? 32 : G);
   return launch_decompress(plan, a, static_cast<cudaStream_t>(stream));
 }

@@ -43,8 +43,10 @@ template <bool UNIFORM, int R>
 __device__ __forceinline__ uint32_t strip_word(const PlanView& pv, uint32_t x, uint32_t w,
                                                uint32_t m) {
   if constexpr (UNIFORM) {
-    if constexpr (R > 0) return extract_runs<R>(x, pv.u_rmask, pv.u_rsh);
-    return compress5(x, pv.u_mv, pv.u_keep);
+    if constexpr (R > 0)
+      return extract_runs<R>(x, pv.u_rmask, pv.u_rsh);
+    else
+      return compress5(x, pv.u_mv, pv.u_keep);
   } else {
     const uint32_t W = pv.W;
     if constexpr (R > 0) {
@@ -56,16 +58,17 @@ __device__ __forceinline__ uint32_t strip_word(const PlanView& pv, uint32_t x, u
         rs[k] = (sh >> (8 * k)) & 0xFFu;
       }
       return extract_runs<R>(x, rm, rs);
-    }
-    uint32_t mv[5];
+    } else {
+      uint32_t mv[5];
 #pragma unroll
-    for (int i = 0; i < 5; ++i) mv[i] = __ldg(pv.mv + i * W + w);
-    return compress5(x, mv, ~m);
+      for (int i = 0; i < 5; ++i) mv[i] = __ldg(pv.mv + i * W + w);
+      return compress5(x, mv, ~m);
+    }
   }
 }
 
 template <bool UNIFORM, int R>
-__global__ void __launch_bounds__(kCompWarpsMax * 32) k_compress(const CompressArgs a) {
+__global__ void __launch_bounds__(kCompWarpsMax * 32, 2) k_compress(const CompressArgs a) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;

@@ -37,8 +37,10 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 template <bool UNIFORM, int R>
 __device__ __forceinline__ uint32_t rebuild_word(const PlanView& pv, uint32_t v, uint32_t w) {
   if constexpr (UNIFORM) {
-    if constexpr (R > 0) return deposit_runs<R>(v, pv.u_rmask, pv.u_rsh) | pv.u_bm;
-    return expand5(v, pv.u_mv, pv.u_keep) | pv.u_bm;
+    if constexpr (R > 0)
+      return deposit_runs<R>(v, pv.u_rmask, pv.u_rsh) | pv.u_bm;
+    else
+      return expand5(v, pv.u_mv, pv.u_keep) | pv.u_bm;
   } else {
     const uint32_t W = pv.W;
     if constexpr (R > 0) {
@@ -50,25 +52,25 @@ __device__ __forceinline__ uint32_t rebuild_word(const PlanView& pv, uint32_t v,
         rs[k] = (sh >> (8 * k)) & 0xFFu;
       }
       return deposit_runs<R>(v, rm, rs) | __ldg(pv.bm + w);
-    }
-    uint32_t mv[5];
+    } else {
+      uint32_t mv[5];
 #pragma unroll
-    for (int i = 0; i < 5; ++i) mv[i] = __ldg(pv.mv + i * W + w);
-    return expand5(v, mv, ~__ldg(pv.mask + w)) | __ldg(pv.bm + w);
+      for (int i = 0; i < 5; ++i) mv[i] = __ldg(pv.mv + i * W + w);
+      return expand5(v, mv, ~__ldg(pv.mask + w)) | __ldg(pv.bm + w);
+    }
   }
 }
 
-// Decode one compressed row whose stream words [S, Lw) are in pb and whose
-// S header words are in hb; write its W words to orow.
+// Decode one compressed row whose stream (headers first) is in pb; write its
+// W words to orow.  General form: any W, per-word tables or uniform scalars.
 template <bool UNIFORM, int R>
 __device__ __forceinline__ void decode_row(const PlanView& pv, const uint32_t* __restrict__ pb,
-                                           const uint32_t* __restrict__ hb,
-                                           uint32_t* __restrict__ orow, uint32_t lane) {
+                                           uint32_t* __restrict__ orow, uint32_t lane,
+                                           uint32_t lt) {
   const uint32_t W = pv.W, S = pv.S;
-  const uint32_t lt = lanemask_lt();
   uint32_t base = 32u * S;  // stream bit of segment s's first field
   for (uint32_t s = 0; s < S; ++s) {
-    const uint32_t H = hb[s];
+    const uint32_t H = pb[s];
     const uint32_t w = 32u * s + lane;
     const uint32_t flag = (H >> lane) & 1u;
     uint32_t off, seg;
@@ -98,63 +100,92 @@ __device__ __forceinline__ void decode_row(const PlanView& pv, const uint32_t* _
   }
 }
 
+// Uniform plan, W a multiple of 32: every segment is full and every word has
+// the same Mask, so lane i's field in segment s starts at bit
+//   32 S + 1024 s + 32 i - p * (matching words before it),
+// read with one funnel shift over two shared-memory words.
+template <int R>
+__device__ __forceinline__ void decode_row_fast(const PlanView& pv, const uint32_t* __restrict__ pb,
+                                                uint32_t* __restrict__ orow, uint32_t lane,
+                                                uint32_t lt) {
+  const uint32_t S = pv.S, p = pv.u_p;
+  const uint32_t lanebit = 1u << lane;
+  uint32_t base = 32u * S + 32u * lane;
+  uint32_t* o = orow + lane;
+#pragma unroll 4
+  for (uint32_t s = 0; s < S; ++s) {
+    const uint32_t H = pb[s];
+    const uint32_t P = base - p * __popc(H & lt);
+    const uint32_t* q = pb + (P >> 5);
+    const uint32_t v = __funnelshift_r(q[0], q[1], P);
+    uint32_t y;
+    if constexpr (R > 0)
+      y = deposit_runs<R>(v, pv.u_rmask, pv.u_rsh) | pv.u_bm;
+    else
+      y = expand5(v, pv.u_mv, pv.u_keep) | pv.u_bm;
+    o[32u * s] = (H & lanebit) ? y : v;
+    base += 1024u - p * __popc(H);
+  }
+}
+
 template <bool UNIFORM, int R>
 __global__ void __launch_bounds__(kDecWarpsMax * 32) k_decompress(const DecodeArgs a) {
   extern __shared__ __align__(16) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t nw_cta = blockDim.x >> 5;
-  const uint32_t G = a.G, W = a.pv.W, S = a.pv.S;
-  const uint32_t rowcap = a.rowcap, scap = a.scap;
-  uint32_t* const pbuf = smem + warp * (2u * G * rowcap + 3u * G * scap);  // [2][G][rowcap]
-  uint32_t* const hbuf = pbuf + 2u * G * rowcap;                           // [3][G][scap]
+  const uint32_t G = a.G, W = a.pv.W, S = a.pv.S, rowcap = a.rowcap;
+  // Stage = G rows of rowcap words (a multiple of 32, so a row's 128-byte
+  // global lines land on 128-byte shared-memory lines) plus 32 words for the
+  // decoder's one-word read past the last row.
+  const uint32_t stage_words = G * rowcap + 32u;
+  uint32_t* const stages = smem + warp * 3u * stage_words;  // [3] stages
+  const uint32_t lt = lanemask_lt();
+  const bool fast = UNIFORM && (W & 31u) == 0;
 
   const uint64_t n_groups = (a.n_out + G - 1) / G;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw_cta + warp;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw_cta;
   if (gw >= n_groups) return;  // warp-uniform; only warp-level syncs below
   const uint64_t J = (n_groups - gw + nwarps - 1) / nwarps;
+  // Lane q < G of group j owns output row row_first + j * row_step + q.
+  const uint64_t row_first = gw * G;
+  const uint64_t row_step = nwarps * G;
+  const uint32_t pre = a.pre;
 
-  // Lane q < G of group j owns output row (gw + j * nwarps) * G + q.
-  auto row_index = [&](uint64_t j) -> uint64_t { return (gw + j * nwarps) * G + lane; };
-  auto present = [&](uint64_t j) -> bool { return j < J && lane < G && row_index(j) < a.n_out; };
-
-  auto load_id = [&](uint64_t j) -> int64_t {
-    if (!present(j)) return -1;
-    const uint64_t i = row_index(j);
-    return a.ids ? a.ids[i] : static_cast<int64_t>(a.first + i);
+  auto present = [&](uint64_t j) -> bool {
+    return j < J && lane < G && row_first + j * row_step + lane < a.n_out;
   };
-
   auto in_table = [&](int64_t id) -> bool {
     return id >= 0 && static_cast<uint64_t>(id) < a.n_rows;
   };
-
-  // Headers of group j -> hbuf[hs]; the row's bitmask word -> bmw.
-  auto issue_headers = [&](uint64_t j, uint32_t hs, int64_t id, uint32_t& bmw) {
+  auto load_id = [&](uint64_t j) -> int64_t {
+    if (!present(j)) return -1;
+    const uint64_t i = row_first + j * row_step + lane;
+    return a.ids ? a.ids[i] : static_cast<int64_t>(a.first + i);
+  };
+  // Words [0, pre) of every row of group j (its headers and the part of the
+  // stream that every compressed row has), and the row's bitmask word.
+  auto issue_prefix = [&](uint64_t j, uint32_t* sb, int64_t id, uint32_t& bmw) {
     const bool ok = present(j) && in_table(id);
     if (ok) bmw = ld_u32(a.bitmask + (static_cast<uint64_t>(id) >> 5));
     if (j >= J) return;
-    uint32_t* hb = hbuf + hs * G * scap;
-    const uint32_t per_row = a.vec ? (scap >> 2) : S;
-    const uint32_t total = G * per_row;
-    for (uint32_t t = 0; t < total; t += 32) {
-      const uint32_t c = t + lane;
-      const uint32_t q = min(c / per_row, G - 1);
-      const int64_t idq = __shfl_sync(kFull, id, q);
-      const int okq = __shfl_sync(kFull, static_cast<int>(ok), q);
-      if (c < total && okq) {
-        const uint32_t k = c - q * per_row;
-        const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
-        if (a.vec)
-          cp_async16(hb + q * scap + 4u * k, src + 4u * k);
-        else
-          cp_async4(hb + q * scap + k, src + k);
+    const unsigned long long src_l =
+        reinterpret_cast<unsigned long long>(a.slots + static_cast<uint64_t>(ok ? id : 0) * W);
+    for (uint32_t m = __ballot_sync(kFull, ok); m; m &= m - 1) {
+      const uint32_t q = __ffs(m) - 1;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(__shfl_sync(kFull, src_l, q));
+      uint32_t* dst = sb + q * rowcap;
+      if (a.vec) {
+        for (uint32_t c = lane; c < (pre >> 2); c += 32) cp_async16(dst + 4u * c, src + 4u * c);
+      } else {
+        for (uint32_t k = lane; k < pre; k += 32) cp_async4(dst + k, src + k);
       }
     }
   };
 
-  // Row kind and words to fetch, from the headers of group j (lane q).
-  auto row_info = [&](uint64_t j, uint32_t hs, int64_t id, uint32_t bmw, uint32_t& kind,
+  // Row kind and words to read, from the headers of group j (lane q).
+  auto row_info = [&](uint64_t j, const uint32_t* sb, int64_t id, uint32_t bmw, uint32_t& kind,
                       uint32_t& nt) {
     kind = kNone;
     nt = 0;
@@ -168,9 +199,12 @@ __global__ void __launch_bounds__(kDecWarpsMax * 32) k_decompress(const DecodeAr
       nt = W;
       return;
     }
-    const uint32_t* hb = hbuf + hs * G * scap + lane * scap;
+    const uint32_t* hb = sb + lane * rowcap;
     uint32_t drop = 0;  // sum of popcount(Mask) over the matching words
-    for (uint32_t s = 0; s < S; ++s) {
+    // Lane q starts at header q mod S: rows are rowcap words apart (a
+    // multiple of 32), so reading header s on every lane would hit one bank.
+    uint32_t s = lane % S;
+    for (uint32_t t = 0; t < S; ++t, s = (s + 1 == S) ? 0 : s + 1) {
       const uint32_t H = hb[s];
       if (s == S - 1) {
         const uint32_t nb = W - 32u * s;
@@ -186,7 +220,7 @@ __global__ void __launch_bounds__(kDecWarpsMax * 32) k_decompress(const DecodeAr
         for (int k = 0; k < kPlanes; ++k) drop += __popc(H & __ldg(a.pv.planes + s * kPlanes + k)) << k;
       }
     }
-    if (UNIFORM) drop *= a.pv.u_p;
+    if constexpr (UNIFORM) drop *= a.pv.u_p;
     const uint32_t bits = 32u * (S + W) - drop;
     const uint32_t Lw = (bits + 31u) >> 5;
     if (Lw >= W) {
@@ -197,101 +231,111 @@ __global__ void __launch_bounds__(kDecWarpsMax * 32) k_decompress(const DecodeAr
     nt = Lw;
   };
 
-  // Payload of group j -> pbuf[ps]: stream words [S, Lw) of compressed rows
-  // (from the 16-byte chunk holding word S), the whole slot of raw rows.
-  auto issue_payload = [&](uint64_t j, uint32_t ps, int64_t id, uint32_t kind, uint32_t nt) {
+  // The rest of each row of group j: words [pre, Lw) of a compressed row,
+  // [pre, W) of a raw one.  Usually nothing for dense data.
+  auto issue_rest = [&](uint64_t j, uint32_t* sb, int64_t id, uint32_t kind, uint32_t nt) {
     if (j >= J) return;
-    uint32_t* pb = pbuf + ps * G * rowcap;
-    for (uint32_t q = 0; q < G; ++q) {
-      const uint32_t kq = __shfl_sync(kFull, kind, q);
+    const bool need = (kind == kRaw || kind == kComp) && nt > pre;
+    const uint32_t needmask = __ballot_sync(kFull, need);
+    if (!needmask) return;
+    const unsigned long long src_l =
+        reinterpret_cast<unsigned long long>(a.slots + static_cast<uint64_t>(need ? id : 0) * W);
+    for (uint32_t m = needmask; m; m &= m - 1) {
+      const uint32_t q = __ffs(m) - 1;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(__shfl_sync(kFull, src_l, q));
       const uint32_t ntq = __shfl_sync(kFull, nt, q);
-      const int64_t idq = __shfl_sync(kFull, id, q);
-      if (kq != kRaw && kq != kComp) continue;
-      const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
-      uint32_t* dst = pb + q * rowcap;
+      uint32_t* dst = sb + q * rowcap;
       if (a.vec) {
-        const uint32_t c0 = (kq == kComp) ? (S >> 2) : 0u;
-        const uint32_t c1 = (ntq + 3u) >> 2;
-        for (uint32_t c = c0 + lane; c < c1; c += 32) cp_async16(dst + 4u * c, src + 4u * c);
+        for (uint32_t c = (pre >> 2) + lane; c < ((ntq + 3u) >> 2); c += 32) cp_async16(dst + 4u * c, src + 4u * c);
       } else {
-        const uint32_t k0 = (kq == kComp) ? S : 0u;
-        for (uint32_t k = k0 + lane; k < ntq; k += 32) cp_async4(dst + k, src + k);
+        for (uint32_t k = pre + lane; k < ntq; k += 32) cp_async4(dst + k, src + k);
       }
     }
   };
 
-  auto decode_group = [&](uint64_t j, uint32_t ps, uint32_t hs, uint32_t kind) {
-    const uint32_t* pbg = pbuf + ps * G * rowcap;
-    const uint32_t* hbg = hbuf + hs * G * scap;
-    const uint64_t row0 = (gw + j * nwarps) * G;
-    for (uint32_t q = 0; q < G; ++q) {
-      const uint32_t kq = __shfl_sync(kFull, kind, q);
-      if (kq == kNone) continue;
-      uint32_t* orow = a.out + (row0 + q) * W;
-      const uint32_t* pb = pbg + q * rowcap;
-      if (kq == kComp) {
-        decode_row<UNIFORM, R>(a.pv, pb, hbg + q * scap, orow, lane);
-      } else if (kq == kRaw) {
-        if (a.vec) {
-          for (uint32_t c = lane; c < (W >> 2); c += 32)
-            reinterpret_cast<uint4*>(orow)[c] = reinterpret_cast<const uint4*>(pb)[c];
-        } else {
-          for (uint32_t k = lane; k < W; k += 32) orow[k] = pb[k];
-        }
+  auto decode_group = [&](uint64_t j, const uint32_t* sb, uint32_t kind) {
+    uint32_t* const obase = a.out + (row_first + j * row_step) * W;
+    for (uint32_t m = __ballot_sync(kFull, kind == kComp); m; m &= m - 1) {
+      const uint32_t q = __ffs(m) - 1;
+      if (fast) {
+        decode_row_fast<R>(a.pv, sb + q * rowcap, obase + static_cast<uint64_t>(q) * W, lane, lt);
       } else {
-        for (uint32_t k = lane; k < W; k += 32) orow[k] = 0u;
-        if (lane == 0) record_status(a.pv.status, kq == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
+        decode_row<UNIFORM, R>(a.pv, sb + q * rowcap, obase + static_cast<uint64_t>(q) * W, lane, lt);
       }
+    }
+    for (uint32_t m = __ballot_sync(kFull, kind == kRaw); m; m &= m - 1) {
+      const uint32_t q = __ffs(m) - 1;
+      const uint32_t* pb = sb + q * rowcap;
+      uint32_t* orow = obase + static_cast<uint64_t>(q) * W;
+      if (a.vec) {
+        for (uint32_t c = lane; c < (W >> 2); c += 32)
+          reinterpret_cast<uint4*>(orow)[c] = reinterpret_cast<const uint4*>(pb)[c];
+      } else {
+        for (uint32_t k = lane; k < W; k += 32) orow[k] = pb[k];
+      }
+    }
+    const bool bad = kind == kBadRange || kind == kCorrupt;
+    if (bad) record_status(a.pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
+    for (uint32_t m = __ballot_sync(kFull, bad); m; m &= m - 1) {
+      const uint32_t q = __ffs(m) - 1;
+      uint32_t* orow = obase + static_cast<uint64_t>(q) * W;
+      for (uint32_t k = lane; k < W; k += 32) orow[k] = 0u;
     }
   };
 
-  // Prologue: ids of groups 0..2, headers of 0 and 1, payload of 0.
+  // Pipeline, per iteration j: ids of group j+3 (registers), prefix of group
+  // j+2 (cp.async), kinds of group j+1 from its landed headers and the rest of
+  // its rows (cp.async), decode of group j.  Group j lives in stage j % 3.
+  // Commit order per iteration: prefix(j+2), rest(j+1); so before the rest of
+  // j+1 is issued, prefix(j+1) is complete once at most two groups (rest(j),
+  // prefix(j+2)) are pending, and before the decode of j, rest(j) is complete
+  // once at most two (prefix(j+2), rest(j+1)) are.
   int64_t id0 = load_id(0), id1 = load_id(1), id2 = load_id(2);
+  uint32_t* st0 = stages;                    // stage of group j
+  uint32_t* st1 = stages + stage_words;      // stage of group j + 1
+  uint32_t* st2 = stages + 2 * stage_words;  // stage of group j + 2
   uint32_t bm0 = 0, bm1 = 0;
-  issue_headers(0, 0, id0, bm0);
+  issue_prefix(0, st0, id0, bm0);
   cp_commit();
-  issue_headers(1, 1, id1, bm1);
+  issue_prefix(1, st1, id1, bm1);
   cp_commit();
   cp_wait<1>();
   __syncwarp();
   uint32_t kind0, nt0;
-  row_info(0, 0, id0, bm0, kind0, nt0);
-  issue_payload(0, 0, id0, kind0, nt0);
+  row_info(0, st0, id0, bm0, kind0, nt0);
+  issue_rest(0, st0, id0, kind0, nt0);
   cp_commit();
 
-  // Steady state.  Stage indices: payload j in pbuf[j & 1], headers j in
-  // hbuf[j % 3] (h0 = j % 3, h1 = (j+1) % 3, h2 = (j+2) % 3).
-  uint32_t h0 = 0, h1 = 1, h2 = 2;
   for (uint64_t j = 0; j < J; ++j) {
     const int64_t id3 = load_id(j + 3);
     uint32_t bm2 = 0;
-    issue_headers(j + 2, h2, id2, bm2);
+    issue_prefix(j + 2, st2, id2, bm2);
     cp_commit();
-    cp_wait<2>();  // headers of j+1 have landed
+    cp_wait<2>();
     __syncwarp();
     uint32_t kind1, nt1;
-    row_info(j + 1, h1, id1, bm1, kind1, nt1);
-    issue_payload(j + 1, static_cast<uint32_t>((j + 1) & 1), id1, kind1, nt1);
+    row_info(j + 1, st1, id1, bm1, kind1, nt1);
+    issue_rest(j + 1, st1, id1, kind1, nt1);
     cp_commit();
-    cp_wait<2>();  // payload of j has landed
+    cp_wait<2>();
     __syncwarp();
-    decode_group(j, static_cast<uint32_t>(j & 1), h0, kind0);
+    decode_group(j, st0, kind0);
     __syncwarp();
     id1 = id2;
     id2 = id3;
     bm1 = bm2;
     kind0 = kind1;
-    const uint32_t t = h0;
-    h0 = h1;
-    h1 = h2;
-    h2 = t;
+    uint32_t* const t = st0;
+    st0 = st1;
+    st1 = st2;
+    st2 = t;
   }
   cp_wait<0>();
 }
 
 template <bool U, int R>
 static int launch_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  const size_t per_warp = 4ull * (2ull * a.G * a.rowcap + 3ull * a.G * a.scap);
+  const size_t per_warp = 4ull * 3ull * (a.G * a.rowcap + 32ull);
   const size_t budget = 220ull * 1024;
   size_t warps = budget / per_warp;
   if (warps > static_cast<size_t>(kDecWarpsMax)) warps = kDecWarpsMax;

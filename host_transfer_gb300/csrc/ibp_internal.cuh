@@ -59,6 +59,7 @@ struct ibp_plan {
   int device;
   uint32_t W, S;
   uint32_t uniform, max_runs, min_kept, max_kept;
+  uint32_t lmin;  // min(W, words of the shortest possible compressed stream)
   void* d_block;  // single device allocation holding every table + status
   size_t d_bytes;
   ibp::PlanView view;
@@ -91,8 +92,8 @@ struct DecodeArgs {
   uint64_t n_out;          // rows to produce
   uint32_t* out;
   uint32_t G;              // rows per group
-  uint32_t rowcap;         // payload stage words per row
-  uint32_t scap;           // header stage words per row
+  uint32_t rowcap;         // stage words per row: W rounded up to a multiple of 32
+  uint32_t pre;            // words fetched for every row before its headers are read
   uint32_t vec;            // 16-byte copies allowed
 };
 
@@ -105,7 +106,7 @@ struct CompressArgs {
   uint64_t n_rows;
   uint32_t* bitmask;
   unsigned long long* stored;  // may be null
-  uint32_t rowcap;
+  uint32_t rowcap;  // words per row buffer: W rounded up to a multiple of 32
   uint32_t vec;
 };
 

@@ -120,6 +120,7 @@ struct PlanSummary {
   uint32_t max_runs;
   uint32_t min_kept;
   uint32_t max_kept;
+  unsigned long long sum_kept;  // kept bits over all word positions
 };
 
 // One thread per word position; one warp per 32-word segment (for the bit
@@ -175,6 +176,7 @@ __global__ void k_plan_tables(PlanView v, PlanSummary* sum) {
     atomicMax(&sum->max_runs, nruns);
     atomicMin(&sum->min_kept, 32u - p);
     atomicMax(&sum->max_kept, 32u - p);
+    atomicAdd(&sum->sum_kept, static_cast<unsigned long long>(32u - p));
     if (m != mask[0] || b != (bm[0] & mask[0])) atomicOr(&sum->nonuniform, 1u);
   }
   // bit planes of popcount(Mask) per segment
@@ -188,7 +190,7 @@ __global__ void k_plan_tables(PlanView v, PlanSummary* sum) {
 }
 
 int build_plan_tables(ibp_plan* plan) {
-  PlanSummary h = {0, 0, 32, 0};
+  PlanSummary h = {0, 0, 32, 0, 0};
   PlanSummary* d = nullptr;
   cudaError_t e = cudaMalloc(&d, sizeof(PlanSummary));
   if (e != cudaSuccess) {
@@ -213,6 +215,11 @@ int build_plan_tables(ibp_plan* plan) {
   plan->max_runs = h.max_runs;
   plan->min_kept = h.min_kept;
   plan->max_kept = h.max_kept;
+  // Shortest stream a compressed row can have (every word matching): the
+  // words a reader needs for any row, whatever its headers say.
+  const uint64_t min_bits = 32ull * plan->S + h.sum_kept;
+  const uint64_t lmin = (min_bits + 31) / 32;
+  plan->lmin = static_cast<uint32_t>(lmin < plan->W ? lmin : plan->W);
   PlanView& v = plan->view;
   // word 0's entries become the uniform scalars (used only when uniform)
   uint32_t w0[13];
