@@ -192,6 +192,17 @@ def workload_desc(name: str, n_rows: int) -> str:
     }[name]
 
 
+def graph_of(torch, fn, count, first, pool):
+    """Capture fn(k) for k = first .. first + count - 1 (batch k mod pool) as
+    one CUDA graph, so the timed steps run back to back on the GPU with no
+    host enqueue time between them."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        for k in range(count):
+            fn((first + k) % pool)
+    return g
+
+
 def make_batches(name, n_rows, count, offset):
     from host_transfer_gb300 import workloads
 
@@ -339,20 +350,21 @@ def run_ours(args):
     h2d_gbs = statistics.median(h2d)
 
     def time_steps(fn, count, first):
+        """Warm up eagerly, then time `count` steps replayed as a CUDA graph."""
+        for k in range(WU):
+            fn(k % pool)
+        g = graph_of(torch, fn, count, first, pool)
+        g.replay()  # untimed first replay
+        torch.cuda.synchronize(dev)
         a, b = ev(), ev()
         a.record(stream)
-        for k in range(count):
-            fn((first + k) % pool)
+        g.replay()
         b.record(stream)
         torch.cuda.synchronize(dev)
         return a.elapsed_time(b)
 
     # uncompressed gathers of the same rows: zero copy from host, and from HBM
-    for k in range(WU):
-        ibp.ibp_gather_raw(table, ids_d[k % pool], out=out)
     raw_host_ms = time_steps(lambda k: ibp.ibp_gather_raw(table, ids_d[k], out=out), K, WU)
-    for k in range(WU):
-        ibp.ibp_gather_raw(table_d, ids_d[k % pool], out=out)
     raw_hbm_ms = time_steps(lambda k: ibp.ibp_gather_raw(table_d, ids_d[k], out=out), K, WU)
 
     # compress in place on the pinned table (step 2, zero copy)
@@ -375,8 +387,19 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     # ---- timed region: host-resident gather-decompress -------------------
-    starts = [ev() for _ in range(K)]
-    ends = [ev() for _ in range(K)]
+    # K steps captured once as a CUDA graph (launch-bound loops belong in
+    # graphs); the replay is the timed region.
+    def dec_host(k):
+        ibp.ibp_gather_decompress(plan, table, bitmask, ids_d[k], out=out)
+
+    def dec_hbm(k):
+        ibp.ibp_gather_decompress(plan, table_d, bitmask, ids_d[k], out=out)
+
+    for k in range(WU):
+        dec_host(k % pool)
+    ibp.ibp_get_status(plan)
+    g_host = graph_of(torch, dec_host, K, WU, pool)
+    g_hbm = graph_of(torch, dec_hbm, K, WU, pool)
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -389,50 +412,43 @@ def run_ours(args):
     t_soak = time.perf_counter()
     k = 0
     while time.perf_counter() - t_soak < SOAK_S:  # untimed: clocks settle under this load
-        ibp.ibp_gather_decompress(plan, table, bitmask, ids_d[k % pool], out=out)
+        dec_host(k % pool)
         k += 1
         if k % 64 == 0:
             torch.cuda.synchronize(dev)
     for k in range(WU):
-        ibp.ibp_gather_decompress(plan, table, bitmask, ids_d[k % pool], out=out)
+        dec_host(k % pool)
     torch.cuda.synchronize(dev)
-    ibp.ibp_get_status(plan)
     g0, g1 = ev(), ev()
     torch.cuda.nvtx.range_push("host_timed")  # ncu --nvtx --nvtx-include host_timed/
     g0.record(stream)
-    for k in range(K):
-        starts[k].record(stream)
-        ibp.ibp_gather_decompress(plan, table, bitmask, ids_d[(WU + k) % pool], out=out)
-        ends[k].record(stream)
+    g_host.replay()
     g1.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
     total_ms = g0.elapsed_time(g1)
-    launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    launch_ms = total_ms / K
     ibp.ibp_get_status(plan)
     parity = bool(np.array_equal(out.cpu().numpy().view(np.uint32), expect_last))
 
     # ---- HBM-resident gather-decompress -----------------------------------
     for k in range(WU):
-        ibp.ibp_gather_decompress(plan, table_d, bitmask, ids_d[k % pool], out=out)
-    hs = [ev() for _ in range(K)]
-    he = [ev() for _ in range(K)]
+        dec_hbm(k % pool)
+    torch.cuda.synchronize(dev)
     a, b = ev(), ev()
     torch.cuda.nvtx.range_push("hbm_timed")  # ncu --nvtx --nvtx-include hbm_timed/
     a.record(stream)
-    for k in range(K):
-        hs[k].record(stream)
-        ibp.ibp_gather_decompress(plan, table_d, bitmask, ids_d[(WU + k) % pool], out=out)
-        he[k].record(stream)
+    g_hbm.replay()
     b.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     hbm_total_ms = a.elapsed_time(b)
-    hbm_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(hs, he))
+    hbm_launch_ms = hbm_total_ms / K
     ibp.ibp_get_status(plan)
     parity = parity and bool(np.array_equal(out.cpu().numpy().view(np.uint32), expect_last))
+    del g_host, g_hbm
 
     # ---- end to end through the public API ----------------------------------
     ids_host = torch.from_numpy(batches).pin_memory()
@@ -504,6 +520,7 @@ def run_ours(args):
         "clocks": clocks,
         "table_gen_s": round(gen_s, 2),
         "id_batches": f"{pool} distinct batches, step k uses batch k mod {pool}",
+        "timing": "K steps captured as one CUDA graph, replay timed with CUDA events; e2e: eager API calls",
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -187,24 +187,24 @@ static int launch_t(const ibp_plan* plan, CompressArgs& a, cudaStream_t stream) 
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = warps * per_warp;
   auto kern = k_compress<U, R>;
-  static bool attr_set[64] = {false};
+  // One-time set-up per device: the shared-memory opt-in and the occupancy
+  // for this launch shape (smem depends only on the row width).
+  static int occ_cache[64] = {0};
+  static size_t occ_smem[64] = {0};
   const int dev = plan->device;
   if (dev < 0 || dev >= 64) return IBP_EINVAL;
-  if (!attr_set[dev]) {
+  int occ = occ_cache[dev];
+  if (occ == 0 || occ_smem[dev] != smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) {
-      set_cuda_error(e, "cudaFuncSetAttribute(k_compress)");
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, static_cast<int>(warps * 32), smem);
+    if (e != cudaSuccess || occ < 1) {
+      set_cuda_error(e, "set-up of k_compress");
       cudaGetLastError();
       return IBP_ECUDA;
     }
-    attr_set[dev] = true;
-  }
-  int occ = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, static_cast<int>(warps * 32), smem);
-  if (e != cudaSuccess || occ < 1) {
-    set_cuda_error(e, "occupancy(k_compress)");
-    cudaGetLastError();
-    return IBP_ECUDA;
+    occ_cache[dev] = occ;
+    occ_smem[dev] = smem;
   }
   const uint64_t blocks32 = (a.n_rows + 31) / 32;
   const uint64_t need = (blocks32 + warps - 1) / warps;

@@ -342,24 +342,24 @@ static int launch_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = warps * per_warp;
   auto kern = k_decompress<U, R>;
-  static bool attr_set[64] = {false};
+  // One-time set-up per device: the shared-memory opt-in and the occupancy
+  // for this launch shape (smem depends only on the row width).
+  static int occ_cache[64] = {0};
+  static size_t occ_smem[64] = {0};
   const int dev = plan->device;
   if (dev < 0 || dev >= 64) return IBP_EINVAL;
-  if (!attr_set[dev]) {
+  int occ = occ_cache[dev];
+  if (occ == 0 || occ_smem[dev] != smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) {
-      set_cuda_error(e, "cudaFuncSetAttribute(k_decompress)");
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, static_cast<int>(warps * 32), smem);
+    if (e != cudaSuccess || occ < 1) {
+      set_cuda_error(e, "set-up of k_decompress");
       cudaGetLastError();
       return IBP_ECUDA;
     }
-    attr_set[dev] = true;
-  }
-  int occ = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, static_cast<int>(warps * 32), smem);
-  if (e != cudaSuccess || occ < 1) {
-    set_cuda_error(e, "occupancy(k_decompress)");
-    cudaGetLastError();
-    return IBP_ECUDA;
+    occ_cache[dev] = occ;
+    occ_smem[dev] = smem;
   }
   const uint64_t groups = (a.n_out + a.G - 1) / a.G;
   const uint64_t need = (groups + warps - 1) / warps;
@@ -370,6 +370,7 @@ static int launch_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
 }
 
 int launch_decompress(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  if (fast_decompress_applies(plan, a)) return launch_decompress_fast(plan, a, stream);
   const uint32_t runs = plan->max_runs;
   const int R = runs <= static_cast<uint32_t>(kMaxRuns) ? (runs == 0 ? 1 : static_cast<int>(runs)) : 0;
   if (plan->uniform) {

@@ -1,0 +1,308 @@
+// ibp_decompress_fast.cu - gather/contiguous decompress specialised for the
+// common plan shape: every word position shares one Mask/Bitval (uniform
+// plan), rows are a whole number of 32-word segments (W = 32 * SC), the
+// kept bits form at most four runs, buffers are 16-byte aligned and row ids
+// fit in 31 bits.  The method is the same as k_decompress (« Algorithme
+// central », step 3: a warp stages a row's compressed segment in shared
+// memory, computes each lane's bit offset with warp primitives and puts the
+// Bitval bits back); what changes is that W, the rows per group G and the
+// segment count are compile-time constants, so every loop unrolls, headers
+// are read with 16-byte shared loads, the deposit constants sit in
+// registers, and the prefetch maps lane i to 16-byte chunk i of each row.
+//
+// Pipeline per warp (as in k_decompress): ids of group j+3 -> registers;
+// prefix [0, pre) of the G rows of group j+2 -> shared stage (cp.async);
+// kinds of group j+1 from its landed headers, then the rest [pre, Lw) of
+// its rows -> shared stage (cp.async); decode of group j.  Stages are G rows
+// of W words (W a multiple of 32: a row's 128-byte global lines land on
+// 128-byte shared-memory lines) plus 32 words for the decoder's read of one
+// word past a row.
+#include <cuda_runtime.h>
+
+#include "ibp_internal.cuh"
+
+namespace ibp {
+
+constexpr int kFastWarps = 8;
+constexpr uint32_t kAll = 0xFFFFFFFFu;
+
+template <int SC>
+struct FastShape {
+  static constexpr uint32_t W = 32u * SC;
+  static constexpr uint32_t G = SC >= 32 ? 1u : 32u / SC;  // rows per group: G * W <= 1024 words
+  static constexpr uint32_t STAGE = G * W + 32u;           // words per stage
+  static constexpr uint32_t CH = W / 4;                    // 16-byte chunks per row
+  static constexpr uint32_t CB = (CH + 31) / 32;           // chunk blocks of 32 per row
+};
+
+template <int R, int SC>
+__global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const DecodeArgs a) {
+  using F = FastShape<SC>;
+  constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
+  extern __shared__ __align__(128) uint32_t smem[];
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t nw_cta = blockDim.x >> 5;
+  uint32_t* const stages = smem + warp * 3u * STAGE;
+  const uint32_t lt = lanemask_lt();
+  const uint32_t lanebit = 1u << lane;
+
+  // plan constants
+  const uint32_t p = a.pv.u_p, bm = a.pv.u_bm;
+  uint32_t rm[R], rs[R];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    rm[k] = a.pv.u_rmask[k];
+    rs[k] = a.pv.u_rsh[k];
+  }
+  const uint32_t pre = a.pre;          // multiple of 4, <= W
+  const uint32_t pre_ch = pre >> 2;    // prefix chunks per row
+  const uint32_t n_rows32 = static_cast<uint32_t>(a.n_rows);  // < 2^31 (checked by the launcher)
+
+  // Warp gw owns groups gw, gw + nwarps, ...; group g is output rows
+  // g*G .. g*G + G - 1 and lane q < G owns row g*G + q.
+  const uint64_t n_groups = (a.n_out + G - 1) / G;
+  const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw_cta + warp;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw_cta;
+  if (gw >= n_groups) return;  // warp-uniform; only warp-level syncs below
+  const uint64_t J = (n_groups - gw + nwarps - 1) / nwarps;
+  const uint64_t row_step = nwarps * G;  // first row of group j+1 minus first row of group j
+
+  // Row ids are carried as 32-bit values; -1 marks "no row" (past the end of
+  // the output) and kBadId an id outside [0, n_rows).
+  constexpr int32_t kNoRow = -1, kBadId = -2;
+  auto load_id = [&](uint64_t j, uint64_t rbase) -> int32_t {
+    const uint64_t i = rbase + lane;
+    if (j >= J || lane >= G || i >= a.n_out) return kNoRow;
+    const int64_t id = a.ids ? a.ids[i] : static_cast<int64_t>(a.first + i);
+    return (id >= 0 && static_cast<uint64_t>(id) < n_rows32) ? static_cast<int32_t>(id) : kBadId;
+  };
+
+  // Prefix of group j: lane i copies chunk i (+32 ...) of every row.
+  auto issue_prefix = [&](uint64_t j, uint32_t* sb, int32_t id, uint32_t& bmw) {
+    if (id >= 0) bmw = ld_u32(a.bitmask + (static_cast<uint32_t>(id) >> 5));
+    if (j >= J) return;
+#pragma unroll
+    for (uint32_t q = 0; q < G; ++q) {
+      const int32_t idq = __shfl_sync(kAll, id, q);
+      if (idq >= 0) {
+        const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
+        uint32_t* dst = sb + q * W;
+#pragma unroll
+        for (uint32_t b = 0; b < CB; ++b) {
+          const uint32_t c = lane + 32u * b;
+          if (c < pre_ch) cp_async16(dst + 4u * c, src + 4u * c);
+        }
+      }
+    }
+  };
+
+  // Kind and stream length of lane q's row of group j (headers in stage).
+  auto row_info = [&](const uint32_t* sb, int32_t id, uint32_t bmw, uint32_t& kind, uint32_t& nt) {
+    kind = kNone;
+    nt = 0;
+    if (id == kNoRow) return;
+    if (id == kBadId) {
+      kind = kBadRange;
+      return;
+    }
+    if (!((bmw >> (static_cast<uint32_t>(id) & 31u)) & 1u)) {
+      kind = kRaw;
+      nt = W;
+      return;
+    }
+    const uint32_t* hb = sb + lane * W;
+    uint32_t m = 0;  // matching words
+    if constexpr (SC >= 4) {
+#pragma unroll
+      for (int s = 0; s < SC; s += 4) {
+        const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
+        m += __popc(h.x) + __popc(h.y) + __popc(h.z) + __popc(h.w);
+      }
+    } else {
+#pragma unroll
+      for (int s = 0; s < SC; ++s) m += __popc(hb[s]);
+    }
+    const uint32_t Lw = (32u * (SC + W) - p * m + 31u) >> 5;
+    if (Lw >= W) {
+      kind = kCorrupt;
+      return;
+    }
+    kind = kComp;
+    nt = Lw;
+  };
+
+  // Rest of group j: [pre, Lw) of compressed rows, [pre, W) of raw rows.
+  auto issue_rest = [&](uint64_t j, uint32_t* sb, int32_t id, uint32_t kind, uint32_t nt) {
+    if (j >= J) return;
+    const bool need = (kind == kRaw || kind == kComp) && nt > pre;
+    for (uint32_t mk = __ballot_sync(kAll, need); mk; mk &= mk - 1) {
+      const uint32_t q = __ffs(mk) - 1;
+      const int32_t idq = __shfl_sync(kAll, id, q);
+      const uint32_t ntq = __shfl_sync(kAll, nt, q);
+      const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
+      uint32_t* dst = sb + q * W;
+      for (uint32_t c = pre_ch + lane; c < ((ntq + 3u) >> 2); c += 32) cp_async16(dst + 4u * c, src + 4u * c);
+    }
+  };
+
+  auto decode_row = [&](const uint32_t* pb, uint32_t* o) {
+    uint32_t base = 32u * SC + 32u * lane;
+    auto seg = [&](uint32_t H, uint32_t s) {
+      const uint32_t P = base - p * __popc(H & lt);
+      const uint32_t* q = pb + (P >> 5);
+      const uint32_t v = __funnelshift_r(q[0], q[1], P);
+      const uint32_t y = deposit_runs<R>(v, rm, rs) | bm;
+      o[32u * s] = (H & lanebit) ? y : v;
+      base += 1024u - p * __popc(H);
+    };
+    if constexpr (SC >= 4) {
+#pragma unroll
+      for (uint32_t s = 0; s < SC; s += 4) {
+        const uint4 h = *reinterpret_cast<const uint4*>(pb + s);
+        seg(h.x, s);
+        seg(h.y, s + 1);
+        seg(h.z, s + 2);
+        seg(h.w, s + 3);
+      }
+    } else {
+#pragma unroll
+      for (uint32_t s = 0; s < SC; ++s) seg(pb[s], s);
+    }
+  };
+
+  auto decode_group = [&](const uint32_t* sb, uint64_t rbase, uint32_t kind) {
+    uint32_t* const obase = a.out + rbase * W + lane;
+    const uint32_t comp = __ballot_sync(kAll, kind == kComp);
+    const uint32_t raw = __ballot_sync(kAll, kind == kRaw);
+    const bool bad = kind == kBadRange || kind == kCorrupt;
+    const uint32_t badm = __ballot_sync(kAll, bad);
+#pragma unroll
+    for (uint32_t q = 0; q < G; ++q) {
+      if ((comp >> q) & 1u) decode_row(sb + q * W, obase + q * W);
+    }
+    if (raw | badm) {
+      if (bad) record_status(a.pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
+      for (uint32_t q = 0; q < G; ++q) {
+        const bool r = (raw >> q) & 1u, z = (badm >> q) & 1u;
+        if (!(r | z)) continue;
+        uint32_t* orow = obase - lane + q * W;
+        const uint4* prow = reinterpret_cast<const uint4*>(sb + q * W);
+#pragma unroll
+        for (uint32_t b = 0; b < CB; ++b) {
+          const uint32_t c = lane + 32u * b;
+          if (c < F::CH) reinterpret_cast<uint4*>(orow)[c] = r ? prow[c] : make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+  };
+
+  // Pipeline: commit order per iteration is prefix(j+2), rest(j+1); see
+  // k_decompress for the wait arithmetic.
+  uint64_t rb0 = gw * G;  // first output row of group j
+  int32_t id0 = load_id(0, rb0), id1 = load_id(1, rb0 + row_step), id2 = load_id(2, rb0 + 2 * row_step);
+  uint32_t* st0 = stages;
+  uint32_t* st1 = stages + STAGE;
+  uint32_t* st2 = stages + 2 * STAGE;
+  uint32_t bm0 = 0, bm1 = 0;
+  issue_prefix(0, st0, id0, bm0);
+  cp_commit();
+  issue_prefix(1, st1, id1, bm1);
+  cp_commit();
+  cp_wait<1>();
+  __syncwarp();
+  uint32_t kind0, nt0;
+  row_info(st0, id0, bm0, kind0, nt0);
+  issue_rest(0, st0, id0, kind0, nt0);
+  cp_commit();
+
+  for (uint64_t j = 0; j < J; ++j, rb0 += row_step) {
+    const int32_t id3 = load_id(j + 3, rb0 + 3 * row_step);
+    uint32_t bm2 = 0;
+    issue_prefix(j + 2, st2, id2, bm2);
+    cp_commit();
+    cp_wait<2>();
+    __syncwarp();
+    uint32_t kind1, nt1;
+    row_info(st1, id1, bm1, kind1, nt1);
+    issue_rest(j + 1, st1, id1, kind1, nt1);
+    cp_commit();
+    cp_wait<2>();
+    __syncwarp();
+    decode_group(st0, rb0, kind0);
+    __syncwarp();
+    id1 = id2;
+    id2 = id3;
+    bm1 = bm2;
+    kind0 = kind1;
+    uint32_t* const t = st0;
+    st0 = st1;
+    st1 = st2;
+    st2 = t;
+  }
+  cp_wait<0>();
+}
+
+template <int R, int SC>
+static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  using F = FastShape<SC>;
+  const size_t per_warp = 4ull * 3ull * F::STAGE;
+  const size_t smem = kFastWarps * per_warp;
+  auto kern = k_decompress_fast<R, SC>;
+  // One-time set-up per device: the shared-memory opt-in and the occupancy
+  // for this launch shape (smem depends only on the row width).
+  static int occ_cache[64] = {0};
+  static size_t occ_smem[64] = {0};
+  const int dev = plan->device;
+  if (dev < 0 || dev >= 64) return IBP_EINVAL;
+  int occ = occ_cache[dev];
+  if (occ == 0 || occ_smem[dev] != smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kFastWarps * 32, smem);
+    if (e != cudaSuccess || occ < 1) {
+      set_cuda_error(e, "set-up of k_decompress_fast");
+      cudaGetLastError();
+      return IBP_ECUDA;
+    }
+    occ_cache[dev] = occ;
+    occ_smem[dev] = smem;
+  }
+  const uint64_t groups = (a.n_out + F::G - 1) / F::G;  // warps that would each get one group
+  const uint64_t need = (groups + kFastWarps - 1) / kFastWarps;
+  const uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
+  const unsigned grid = static_cast<unsigned>(need < cap ? need : cap);
+  kern<<<grid, kFastWarps * 32, smem, stream>>>(a);
+  return check_launch("k_decompress_fast");
+}
+
+template <int R>
+static int launch_fast_r(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  switch (plan->S) {
+    case 1: return launch_fast_t<R, 1>(plan, a, stream);
+    case 2: return launch_fast_t<R, 2>(plan, a, stream);
+    case 4: return launch_fast_t<R, 4>(plan, a, stream);
+    case 8: return launch_fast_t<R, 8>(plan, a, stream);
+    case 16: return launch_fast_t<R, 16>(plan, a, stream);
+    case 32: return launch_fast_t<R, 32>(plan, a, stream);
+    default: return launch_fast_t<R, 64>(plan, a, stream);
+  }
+}
+
+bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a) {
+  const uint32_t S = plan->S;
+  const bool pow2_segments = S == 1 || S == 2 || S == 4 || S == 8 || S == 16 || S == 32 || S == 64;
+  return plan->uniform && plan->max_runs >= 1 && plan->max_runs <= static_cast<uint32_t>(kMaxRuns) &&
+         plan->W == 32u * S && pow2_segments && a.vec && a.n_rows < (1ull << 31) && (a.pre % 4u) == 0;
+}
+
+int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  switch (plan->max_runs) {
+    case 1: return launch_fast_r<1>(plan, a, stream);
+    case 2: return launch_fast_r<2>(plan, a, stream);
+    case 3: return launch_fast_r<3>(plan, a, stream);
+    default: return launch_fast_r<4>(plan, a, stream);
+  }
+}
+
+}  // namespace ibp

@@ -98,6 +98,11 @@ struct DecodeArgs {
 };
 
 int launch_decompress(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+// Specialised decompress for uniform plans with W = 32 * 2^k <= 2048 words,
+// at most kMaxRuns runs of kept bits, 16-byte aligned buffers and fewer than
+// 2^31 rows (ibp_decompress_fast.cu).
+bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a);
+int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 
 struct CompressArgs {
   PlanView pv;

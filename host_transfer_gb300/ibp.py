@@ -119,6 +119,23 @@ def _rows(t: torch.Tensor):
     return w, w.shape[0], w.shape[1]
 
 
+def _word_rows(t: torch.Tensor):
+    """(data pointer, rows, words per row) of a contiguous word tensor, without
+    building views (the per-call path of the gather entry points)."""
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    es = t.element_size()
+    last = t.shape[-1] if t.dim() else 1
+    if es == 4:
+        W = last
+    elif es == 2 and last % 2 == 0:
+        W = last // 2
+    else:
+        raise ValueError(f"unsupported dtype {t.dtype} / row length")
+    n = (t.numel() * es) // (4 * W) if W else 0
+    return ctypes.c_void_p(t.data_ptr()), n, W
+
+
 def _stream(stream, device) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream(device)
@@ -246,35 +263,31 @@ def ibp_gather_decompress(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor
                           row_ids: torch.Tensor, out: torch.Tensor | None = None, stream=None,
                           n_rows: int | None = None) -> torch.Tensor:
     lib = load()
-    s, n, W = _rows(slots)
+    sp, n, W = _word_rows(slots)
     if W != plan.W:
         raise ValueError(f"slots have {W} words, plan has {plan.W}")
     if row_ids.dtype != torch.int64 or not row_ids.is_contiguous():
         raise ValueError("row_ids must be a contiguous int64 tensor")
-    dev = torch.device("cuda", plan.device)
     k = row_ids.numel()
     if out is None:
-        out = torch.empty((k, W), dtype=torch.int32, device=dev)
-    with torch.cuda.device(dev):
-        _check(lib.ibp_gather_decompress(plan.handle, _ptr(s), n if n_rows is None else n_rows,
-                                         _ptr(bitmask), _ptr(row_ids), k, _ptr(out),
-                                         _stream(stream, dev)), "ibp_gather_decompress")
+        out = torch.empty((k, W), dtype=torch.int32, device=torch.device("cuda", plan.device))
+    _check(lib.ibp_gather_decompress(plan.handle, sp, n if n_rows is None else n_rows,
+                                     _ptr(bitmask), _ptr(row_ids), k, _ptr(out),
+                                     _stream(stream, plan.device)), "ibp_gather_decompress")
     return out
 
 
 def ibp_decompress_contig(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, first_row: int,
                           n: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     lib = load()
-    s, n_rows, W = _rows(slots)
+    sp, n_rows, W = _word_rows(slots)
     if W != plan.W:
         raise ValueError(f"slots have {W} words, plan has {plan.W}")
-    dev = torch.device("cuda", plan.device)
     if out is None:
-        out = torch.empty((n, W), dtype=torch.int32, device=dev)
-    with torch.cuda.device(dev):
-        _check(lib.ibp_decompress_contig(plan.handle, _ptr(s), n_rows, _ptr(bitmask), int(first_row),
-                                         int(n), _ptr(out), _stream(stream, dev)),
-               "ibp_decompress_contig")
+        out = torch.empty((n, W), dtype=torch.int32, device=torch.device("cuda", plan.device))
+    _check(lib.ibp_decompress_contig(plan.handle, sp, n_rows, _ptr(bitmask), int(first_row), int(n),
+                                     _ptr(out), _stream(stream, plan.device)),
+           "ibp_decompress_contig")
     return out
 
 
@@ -305,12 +318,11 @@ def ibp_row_lengths(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_
 def ibp_gather_raw(rows: torch.Tensor, row_ids: torch.Tensor, out: torch.Tensor | None = None,
                    stream=None) -> torch.Tensor:
     lib = load()
-    r, n, W = _rows(rows)
+    rp, n, W = _word_rows(rows)
     dev = _device_of(row_ids, out)
     k = row_ids.numel()
     if out is None:
         out = torch.empty((k, W), dtype=torch.int32, device=dev)
-    with torch.cuda.device(dev):
-        _check(lib.ibp_gather_raw(_ptr(r), n, W, _ptr(row_ids), k, _ptr(out), _stream(stream, dev)),
-               "ibp_gather_raw")
+    _check(lib.ibp_gather_raw(rp, n, W, _ptr(row_ids), k, _ptr(out), _stream(stream, dev)),
+           "ibp_gather_raw")
     return out
