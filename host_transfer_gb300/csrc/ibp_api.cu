@@ -153,8 +153,8 @@ int ibp_plan_create(const uint32_t* mask, const uint32_t* bitval, uint32_t W, in
   p->W = W;
   p->S = (W + 31) / 32;
   // Layout (words): mask, bm, pcnt, rmask[4], rshift, mv[5] = 13 W; planes 6 S;
-  // status 1 (padded to 4).
-  const size_t words = 13ull * W + 6ull * p->S + 4;
+  // eplanes 6 S; status 1 (padded to 4).
+  const size_t words = 13ull * W + 12ull * p->S + 4;
   p->d_bytes = words * 4;
   cudaError_t e = cudaMalloc(&p->d_block, p->d_bytes);
   if (e != cudaSuccess) {
@@ -173,7 +173,8 @@ int ibp_plan_create(const uint32_t* mask, const uint32_t* bitval, uint32_t W, in
   v.rshift = base + 7ull * W;
   v.mv = base + 8ull * W;
   v.planes = base + 13ull * W;
-  v.status = base + 13ull * W + 6ull * p->S;
+  v.eplanes = base + 13ull * W + 6ull * p->S;
+  v.status = base + 13ull * W + 12ull * p->S;
   // Mask and Bitval go to the mask and bm slots; the table kernel cleans bm.
   e = cudaMemcpy(const_cast<uint32_t*>(v.mask), mask, 4ull * W, cudaMemcpyDefault);
   if (e == cudaSuccess) e = cudaMemcpy(const_cast<uint32_t*>(v.bm), bitval, 4ull * W, cudaMemcpyDefault);

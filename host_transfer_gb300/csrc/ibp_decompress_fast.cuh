@@ -1,8 +1,13 @@
-// ibp_decompress_fast.cu - gather/contiguous decompress specialised for the
-// common plan shape: every word position shares one Mask/Bitval (uniform
-// plan), rows are a whole number of 32-word segments (W = 32 * SC), the
-// kept bits form at most four runs, buffers are 16-byte aligned and row ids
-// fit in 31 bits.  The method is the same as k_decompress (« Algorithme
+// ibp_decompress_fast.cuh - gather/contiguous decompress specialised for the
+// common plan shapes: rows are a whole number of 32-word segments
+// (W = 32 * SC, SC a power of two up to 64), the kept bits of every word
+// form at most four runs, buffers are 16-byte aligned and row ids fit in 31
+// bits.  Two modes: TAB = false, every word position shares one Mask/Bitval
+// (uniform plan), whose constants sit in registers; TAB = true, per-word
+// Masks, whose deposit runs and Bitval are staged once per CTA in shared
+// memory and whose field offsets use the e-planes of the plan (NPL of them).
+// Instantiated by ibp_decompress_fast_u.cu (uniform) and
+// ibp_decompress_fast_t.cu (tables).  The method is the same as k_decompress (« Algorithme
 // central », step 3: a warp stages a row's compressed segment in shared
 // memory, computes each lane's bit offset with warp primitives and puts the
 // Bitval bits back); what changes is that W, the rows per group G and the
@@ -17,6 +22,8 @@
 // of W words (W a multiple of 32: a row's 128-byte global lines land on
 // 128-byte shared-memory lines) plus 32 words for the decoder's read of one
 // word past a row.
+#pragma once
+
 #include <cuda_runtime.h>
 
 #include "ibp_internal.cuh"
@@ -25,6 +32,21 @@ namespace ibp {
 
 constexpr int kFastWarps = 8;
 constexpr uint32_t kAll = 0xFFFFFFFFu;
+
+// Words of a per-word table entry in shared memory: {run masks, packed run
+// shifts, Bitval & Mask}: 4 words for up to two runs, 8 for up to four.
+template <int R>
+struct TabEntry {
+  static constexpr uint32_t EW = R <= 2 ? 4u : 8u;
+};
+
+template <int SC, int R, int NPL, bool TAB>
+struct TabShape {
+  static constexpr uint32_t W = 32u * SC;
+  static constexpr uint32_t ENT = TAB ? W * TabEntry<R>::EW : 0u;
+  static constexpr uint32_t EPL = TAB && NPL > 0 ? ((SC * NPL + 31u) / 32u) * 32u : 0u;
+  static constexpr uint32_t WORDS = ENT + EPL;  // shared words before the warp stages
+};
 
 template <int SC>
 struct FastShape {
@@ -35,25 +57,47 @@ struct FastShape {
   static constexpr uint32_t CB = (CH + 31) / 32;           // chunk blocks of 32 per row
 };
 
-template <int R, int SC>
+template <int R, int SC, int NPL, bool TAB>
 __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const DecodeArgs a) {
   using F = FastShape<SC>;
+  using T = TabShape<SC, R, NPL, TAB>;
   constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
+  constexpr uint32_t EW = TabEntry<R>::EW;
   extern __shared__ __align__(128) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t nw_cta = blockDim.x >> 5;
-  uint32_t* const stages = smem + warp * 3u * STAGE;
+  uint32_t* const tab = smem;             // [W][EW] per-word entries (TAB)
+  uint32_t* const epl = smem + T::ENT;    // [SC][NPL] e-planes (TAB, NPL > 0)
+  uint32_t* const stages = smem + T::WORDS + warp * 3u * STAGE;
   const uint32_t lt = lanemask_lt();
   const uint32_t lanebit = 1u << lane;
 
-  // plan constants
-  const uint32_t p = a.pv.u_p, bm = a.pv.u_bm;
+  // plan constants: uniform Mask (TAB = false) or the per-word tables
+  const uint32_t p = TAB ? a.pv.p_min : a.pv.u_p;
+  const uint32_t pscale = a.pv.p_scale;
+  const uint32_t bm = a.pv.u_bm;
   uint32_t rm[R], rs[R];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
     rm[k] = a.pv.u_rmask[k];
     rs[k] = a.pv.u_rsh[k];
+  }
+  if constexpr (TAB) {
+    // Stage the tables once per CTA; every thread reaches this barrier
+    // before any warp leaves.
+    for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
+      uint32_t* e = tab + w * EW;
+#pragma unroll
+      for (int k = 0; k < (EW == 4 ? 2 : 4); ++k) e[k] = k < R ? __ldg(a.pv.rmask + k * W + w) : 0u;
+      e[EW == 4 ? 2 : 4] = __ldg(a.pv.rshift + w);
+      e[EW == 4 ? 3 : 5] = __ldg(a.pv.bm + w);
+    }
+    if constexpr (NPL > 0) {
+      for (uint32_t i = threadIdx.x; i < SC * NPL; i += blockDim.x)
+        epl[i] = __ldg(a.pv.eplanes + (i / NPL) * kPlanes + (i % NPL));
+    }
+    __syncthreads();
   }
   const uint32_t pre = a.pre;          // multiple of 4, <= W
   const uint32_t pre_ch = pre >> 2;    // prefix chunks per row
@@ -113,17 +157,28 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
     }
     const uint32_t* hb = sb + lane * W;
     uint32_t m = 0;  // matching words
+    uint32_t me = 0;  // sum of e over the matching words (TAB)
+    auto count = [&](uint32_t H, uint32_t s) {
+      m += __popc(H);
+      if constexpr (TAB && NPL > 0) {
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) me += __popc(H & epl[s * NPL + k]) << k;
+      }
+    };
     if constexpr (SC >= 4) {
 #pragma unroll
-      for (int s = 0; s < SC; s += 4) {
+      for (uint32_t s = 0; s < SC; s += 4) {
         const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
-        m += __popc(h.x) + __popc(h.y) + __popc(h.z) + __popc(h.w);
+        count(h.x, s);
+        count(h.y, s + 1);
+        count(h.z, s + 2);
+        count(h.w, s + 3);
       }
     } else {
 #pragma unroll
-      for (int s = 0; s < SC; ++s) m += __popc(hb[s]);
+      for (uint32_t s = 0; s < SC; ++s) count(hb[s], s);
     }
-    const uint32_t Lw = (32u * (SC + W) - p * m + 31u) >> 5;
+    const uint32_t Lw = (32u * (SC + W) - p * m - pscale * me + 31u) >> 5;
     if (Lw >= W) {
       kind = kCorrupt;
       return;
@@ -149,12 +204,40 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   auto decode_row = [&](const uint32_t* pb, uint32_t* o) {
     uint32_t base = 32u * SC + 32u * lane;
     auto seg = [&](uint32_t H, uint32_t s) {
-      const uint32_t P = base - p * __popc(H & lt);
+      uint32_t P = base - p * __popc(H & lt);
+      uint32_t step = 1024u - p * __popc(H);
+      if constexpr (TAB && NPL > 0) {
+        uint32_t e_lt = 0, e_all = 0;
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) {
+          const uint32_t Ek = H & epl[s * NPL + k];
+          e_lt += __popc(Ek & lt) << k;
+          e_all += __popc(Ek) << k;
+        }
+        P -= pscale * e_lt;
+        step -= pscale * e_all;
+      }
       const uint32_t* q = pb + (P >> 5);
       const uint32_t v = __funnelshift_r(q[0], q[1], P);
-      const uint32_t y = deposit_runs<R>(v, rm, rs) | bm;
+      uint32_t y;
+      if constexpr (TAB) {
+        const uint32_t* e = tab + (32u * s + lane) * EW;
+        const uint4 e0 = *reinterpret_cast<const uint4*>(e);
+        if constexpr (EW == 4) {
+          const uint32_t m2[2] = {e0.x, e0.y};
+          const uint32_t s2[2] = {e0.z & 0xFFu, (e0.z >> 8) & 0xFFu};
+          y = deposit_runs<(R < 2 ? R : 2)>(v, m2, s2) | e0.w;
+        } else {
+          const uint4 e1 = *reinterpret_cast<const uint4*>(e + 4);
+          const uint32_t m4[4] = {e0.x, e0.y, e0.z, e0.w};
+          const uint32_t s4[4] = {e1.x & 0xFFu, (e1.x >> 8) & 0xFFu, (e1.x >> 16) & 0xFFu, e1.x >> 24};
+          y = deposit_runs<R>(v, m4, s4) | e1.y;
+        }
+      } else {
+        y = deposit_runs<R>(v, rm, rs) | bm;
+      }
       o[32u * s] = (H & lanebit) ? y : v;
-      base += 1024u - p * __popc(H);
+      base += step;
     };
     if constexpr (SC >= 4) {
 #pragma unroll
@@ -243,66 +326,57 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   cp_wait<0>();
 }
 
-template <int R, int SC>
+template <int R, int SC, int NPL, bool TAB>
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   using F = FastShape<SC>;
+  using T = TabShape<SC, R, NPL, TAB>;
   const size_t per_warp = 4ull * 3ull * F::STAGE;
-  const size_t smem = kFastWarps * per_warp;
-  auto kern = k_decompress_fast<R, SC>;
+  const size_t fixed = 4ull * T::WORDS;
+  size_t warps = (220ull * 1024 - fixed) / per_warp;
+  if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
+  if (warps < 1) return IBP_EINVAL;
+  const size_t smem = fixed + warps * per_warp;
+  auto kern = k_decompress_fast<R, SC, NPL, TAB>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
-  // for this launch shape (smem depends only on the row width).
+  // for this launch shape.
   static int occ_cache[64] = {0};
-  static size_t occ_smem[64] = {0};
   const int dev = plan->device;
   if (dev < 0 || dev >= 64) return IBP_EINVAL;
   int occ = occ_cache[dev];
-  if (occ == 0 || occ_smem[dev] != smem) {
+  if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kFastWarps * 32, smem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, static_cast<int>(warps * 32), smem);
     if (e != cudaSuccess || occ < 1) {
       set_cuda_error(e, "set-up of k_decompress_fast");
       cudaGetLastError();
       return IBP_ECUDA;
     }
     occ_cache[dev] = occ;
-    occ_smem[dev] = smem;
   }
-  const uint64_t groups = (a.n_out + F::G - 1) / F::G;  // warps that would each get one group
-  const uint64_t need = (groups + kFastWarps - 1) / kFastWarps;
+  const uint64_t groups = (a.n_out + F::G - 1) / F::G;
+  const uint64_t need = (groups + warps - 1) / warps;
   const uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
   const unsigned grid = static_cast<unsigned>(need < cap ? need : cap);
-  kern<<<grid, kFastWarps * 32, smem, stream>>>(a);
+  kern<<<grid, static_cast<unsigned>(warps * 32), smem, stream>>>(a);
   return check_launch("k_decompress_fast");
 }
 
-template <int R>
-static int launch_fast_r(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+template <int R, int NPL, bool TAB>
+static int launch_fast_sc(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   switch (plan->S) {
-    case 1: return launch_fast_t<R, 1>(plan, a, stream);
-    case 2: return launch_fast_t<R, 2>(plan, a, stream);
-    case 4: return launch_fast_t<R, 4>(plan, a, stream);
-    case 8: return launch_fast_t<R, 8>(plan, a, stream);
-    case 16: return launch_fast_t<R, 16>(plan, a, stream);
-    case 32: return launch_fast_t<R, 32>(plan, a, stream);
-    default: return launch_fast_t<R, 64>(plan, a, stream);
+    case 1: return launch_fast_t<R, 1, NPL, TAB>(plan, a, stream);
+    case 2: return launch_fast_t<R, 2, NPL, TAB>(plan, a, stream);
+    case 4: return launch_fast_t<R, 4, NPL, TAB>(plan, a, stream);
+    case 8: return launch_fast_t<R, 8, NPL, TAB>(plan, a, stream);
+    case 16: return launch_fast_t<R, 16, NPL, TAB>(plan, a, stream);
+    case 32: return launch_fast_t<R, 32, NPL, TAB>(plan, a, stream);
+    default: return launch_fast_t<R, 64, NPL, TAB>(plan, a, stream);
   }
 }
 
-bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a) {
-  const uint32_t S = plan->S;
-  const bool pow2_segments = S == 1 || S == 2 || S == 4 || S == 8 || S == 16 || S == 32 || S == 64;
-  return plan->uniform && plan->max_runs >= 1 && plan->max_runs <= static_cast<uint32_t>(kMaxRuns) &&
-         plan->W == 32u * S && pow2_segments && a.vec && a.n_rows < (1ull << 31) && (a.pre % 4u) == 0;
-}
-
-int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  switch (plan->max_runs) {
-    case 1: return launch_fast_r<1>(plan, a, stream);
-    case 2: return launch_fast_r<2>(plan, a, stream);
-    case 3: return launch_fast_r<3>(plan, a, stream);
-    default: return launch_fast_r<4>(plan, a, stream);
-  }
-}
+// Instantiated in ibp_decompress_fast_u.cu and ibp_decompress_fast_t.cu.
+int launch_fast_uniform(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+int launch_fast_table(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace ibp

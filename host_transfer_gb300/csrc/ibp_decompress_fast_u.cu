@@ -1,0 +1,31 @@
+// ibp_decompress_fast_u.cu - uniform-plan instantiations of the specialised
+// decompress kernel (ibp_decompress_fast.cuh) and the choice between the
+// specialised kernels and the general one.
+#include "ibp_decompress_fast.cuh"
+
+namespace ibp {
+
+int launch_fast_uniform(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  switch (plan->max_runs) {
+    case 1: return launch_fast_sc<1, 0, false>(plan, a, stream);
+    case 2: return launch_fast_sc<2, 0, false>(plan, a, stream);
+    case 3: return launch_fast_sc<3, 0, false>(plan, a, stream);
+    default: return launch_fast_sc<4, 0, false>(plan, a, stream);
+  }
+}
+
+bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a) {
+  const uint32_t S = plan->S;
+  const bool pow2_segments = S == 1 || S == 2 || S == 4 || S == 8 || S == 16 || S == 32 || S == 64;
+  const bool runs_ok = plan->max_runs >= 1 && plan->max_runs <= static_cast<uint32_t>(kMaxRuns);
+  // per-word tables: W words x 16 or 32 bytes of shared memory per CTA
+  const bool table_ok = plan->uniform || plan->W <= 1024u;
+  return runs_ok && table_ok && plan->W == 32u * S && pow2_segments && a.vec &&
+         a.n_rows < (1ull << 31) && (a.pre % 4u) == 0;
+}
+
+int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  return plan->uniform ? launch_fast_uniform(plan, a, stream) : launch_fast_table(plan, a, stream);
+}
+
+}  // namespace ibp

@@ -36,6 +36,12 @@ enum RowKind : uint32_t { kNone = 0, kRaw = 1, kComp = 2, kBadRange = 3, kCorrup
 //   planes[s*6+k] bit i = bit k of pcnt[32s+i]; lets one lane sum
 //               popcount(Mask) over the matching words of a segment with six
 //               popcounts.
+//   eplanes[s*6+k] bit i = bit k of e_w, w = 32s+i, where
+//               pcnt[w] = p_min + p_scale * e_w (p_min the smallest popcount,
+//               p_scale the gcd of the differences); e_w < 2^npl.  With two
+//               distinct popcounts npl = 1, so a prefix sum of pcnt over the
+//               matching lanes is p_min * popc(H & lt) + p_scale *
+//               popc(H & E_0 & lt).
 struct PlanView {
   uint32_t W, S;
   const uint32_t* mask;
@@ -45,7 +51,9 @@ struct PlanView {
   const uint32_t* rshift;
   const uint32_t* mv;
   const uint32_t* planes;
+  const uint32_t* eplanes;
   uint32_t* status;
+  uint32_t p_min, p_scale, npl;
   // Uniform plans (every word position has the same Mask/Bitval): scalars.
   uint32_t u_mask, u_bm, u_p, u_keep;
   uint32_t u_rmask[kMaxRuns];

@@ -121,6 +121,8 @@ struct PlanSummary {
   uint32_t min_kept;
   uint32_t max_kept;
   unsigned long long sum_kept;  // kept bits over all word positions
+  uint32_t present_lo;          // bit p set: some word has popcount(Mask) = p (p < 32)
+  uint32_t present_hi;          // some word has popcount(Mask) = 32
 };
 
 // One thread per word position; one warp per 32-word segment (for the bit
@@ -177,6 +179,10 @@ __global__ void k_plan_tables(PlanView v, PlanSummary* sum) {
     atomicMin(&sum->min_kept, 32u - p);
     atomicMax(&sum->max_kept, 32u - p);
     atomicAdd(&sum->sum_kept, static_cast<unsigned long long>(32u - p));
+    if (p < 32u)
+      atomicOr(&sum->present_lo, 1u << p);
+    else
+      atomicOr(&sum->present_hi, 1u);
     if (m != mask[0] || b != (bm[0] & mask[0])) atomicOr(&sum->nonuniform, 1u);
   }
   // bit planes of popcount(Mask) per segment
@@ -189,8 +195,31 @@ __global__ void k_plan_tables(PlanView v, PlanSummary* sum) {
   }
 }
 
+// eplanes[s*6+k] bit i = bit k of (pcnt[32s+i] - p_min) / p_scale.
+__global__ void k_plan_eplanes(PlanView v) {
+  const uint32_t w = blockIdx.x * blockDim.x + threadIdx.x;
+  const bool in = w < v.W;
+  const uint32_t e = in ? (v.pcnt[w] - v.p_min) / v.p_scale : 0u;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t seg = w / 32;
+#pragma unroll
+  for (int k = 0; k < kPlanes; ++k) {
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, in && ((e >> k) & 1u));
+    if (lane == 0 && seg < v.S) const_cast<uint32_t*>(v.eplanes)[seg * kPlanes + k] = bal;
+  }
+}
+
+static uint32_t gcd_u32(uint32_t a, uint32_t b) {
+  while (b) {
+    const uint32_t t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
 int build_plan_tables(ibp_plan* plan) {
-  PlanSummary h = {0, 0, 32, 0, 0};
+  PlanSummary h = {0, 0, 32, 0, 0, 0, 0};
   PlanSummary* d = nullptr;
   cudaError_t e = cudaMalloc(&d, sizeof(PlanSummary));
   if (e != cudaSuccess) {
@@ -210,6 +239,33 @@ int build_plan_tables(ibp_plan* plan) {
     set_cuda_error(e, "k_plan_tables");
     cudaGetLastError();
     return IBP_ECUDA;
+  }
+  // popcounts present -> p_min, p_scale (gcd of the differences), npl
+  {
+    PlanView& v = plan->view;
+    uint32_t pmin = 32, pmax = 0, g = 0;
+    for (uint32_t q = 0; q <= 32; ++q) {
+      const bool has = q < 32 ? ((h.present_lo >> q) & 1u) : (h.present_hi & 1u);
+      if (!has) continue;
+      if (q < pmin) pmin = q;
+      if (q > pmax) pmax = q;
+    }
+    for (uint32_t q = pmin; q <= 32; ++q) {
+      const bool has = q < 32 ? ((h.present_lo >> q) & 1u) : (h.present_hi & 1u);
+      if (has && q > pmin) g = gcd_u32(g, q - pmin);
+    }
+    v.p_min = pmin;
+    v.p_scale = g ? g : 1u;
+    const uint32_t emax = (pmax - pmin) / v.p_scale;
+    v.npl = emax == 0 ? 0u : (emax == 1 ? 1u : 6u);
+    k_plan_eplanes<<<(plan->W + 255) / 256, 256>>>(v);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      set_cuda_error(e, "k_plan_eplanes");
+      cudaGetLastError();
+      return IBP_ECUDA;
+    }
   }
   plan->uniform = h.nonuniform ? 0u : 1u;
   plan->max_runs = h.max_runs;

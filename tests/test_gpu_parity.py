@@ -339,3 +339,63 @@ def test_row_lengths_match_oracle_stored_words(W):
     got = lens.cpu().numpy()
     assert got[:200].tolist() == want
     assert got[200] == 0 and got[201] == 0 and got[202] == want[7]
+
+
+def _explicit_plan_check(mask, bitval, rows, where="hbm"):
+    """Compress + gather with an explicit Mask/Bitval; compare with the oracle."""
+    plan = ibp.ibp_plan_create(torch.from_numpy(mask.view(np.int32)), torch.from_numpy(bitval.view(np.int32)))
+    rows_t = place(rows, where)
+    slots_t = empty_like_in(rows_t, where)
+    _, bitmask, stored = ibp.ibp_compress(plan, rows_t, slots_t)
+    n = rows.shape[0]
+    ids = np.random.default_rng(n).integers(0, n, 3 * n).astype(np.int64)
+    out = ibp.ibp_gather_decompress(plan, slots_t, bitmask, torch.from_numpy(ids).cuda())
+    contig = ibp.ibp_decompress_contig(plan, slots_t, bitmask, 3, n - 5)
+    torch.cuda.synchronize()
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+    cs, cb, cst = C.compress(rows, mask, bitval)
+    assert np.array_equal(words_np(slots_t), cs) and np.array_equal(words_np(bitmask), cb)
+    assert int(stored.item()) == cst
+    assert np.array_equal(words_np(out), rows[ids])
+    assert np.array_equal(words_np(contig), rows[3:n - 2])
+    return plan
+
+
+def _rows_for(mask, bitval, rng, n, p_match=0.85):
+    W = mask.size
+    rows = rng.integers(0, 2**32, (n, W), dtype=np.uint64).astype(np.uint32)
+    match = rng.random((n, W)) < p_match
+    rows = np.where(match, (rows & ~mask) | (bitval & mask), rows).astype(np.uint32)
+    return rows
+
+
+def _run_mask(lo, length):
+    return ((1 << length) - 1) << lo
+
+
+@pytest.mark.parametrize("W", [32, 128, 512])
+@pytest.mark.parametrize("kind", ["same_popcount", "two_popcounts", "many_popcounts", "up_to_4_runs"])
+def test_per_word_plans_fast_table_modes(W, kind):
+    """Per-word Masks of the shapes the table kernel specialises for: the same
+    popcount at different positions (no e-plane), two popcounts (one e-plane),
+    many popcounts (six e-planes), and up to four runs of kept bits."""
+    rng = np.random.default_rng(W + len(kind))
+    keep = np.zeros(W, np.uint64)
+    for w in range(W):
+        if kind == "same_popcount":
+            keep[w] = _run_mask(w % 20, 8)  # 8 kept bits, shifting position
+        elif kind == "two_popcounts":
+            keep[w] = _run_mask(0, 27) | (1 << 31) if w % 3 else _run_mask(26, 4)
+        elif kind == "many_popcounts":
+            keep[w] = _run_mask(w % 7, 1 + (w * 5) % 30)
+        else:
+            keep[w] = _run_mask(0, 3) | _run_mask(6, 2) | _run_mask(12, 5) | _run_mask(24, 1 + w % 7)
+    mask = (~keep & 0xFFFFFFFF).astype(np.uint32)
+    bitval = rng.integers(0, 2**32, W, dtype=np.uint64).astype(np.uint32) & mask
+    rows = _rows_for(mask, bitval, rng, 700)
+    rows[::13] = rng.integers(0, 2**32, (len(rows[::13]), W), dtype=np.uint64).astype(np.uint32)
+    plan = _explicit_plan_check(mask, bitval, rows, "hbm")
+    _explicit_plan_check(mask, bitval, rows[:200], "host")
+    assert plan.info["uniform"] == 0
+    if kind == "up_to_4_runs":
+        assert plan.info["max_runs"] == 4
