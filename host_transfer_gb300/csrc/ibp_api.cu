@@ -221,6 +221,12 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out) {
   return IBP_OK;
 }
 
+int ibp_plan_set_hints(ibp_plan* plan, uint32_t hints) {
+  if (!plan || (hints & ~IBP_HINT_ROW_REUSE)) return IBP_EINVAL;
+  plan->view.hints = hints;
+  return IBP_OK;
+}
+
 int ibp_plan_get_mask(const ibp_plan* plan, uint32_t* mask, uint32_t* bitval) {
   if (!plan) return IBP_EINVAL;
   DeviceGuard g(plan->device);

@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kDecWarpsMax * 32) k_decompress(const DecodeAr
   const uint64_t row_first = gw * G;
   const uint64_t row_step = nwarps * G;
   const uint32_t pre = a.pre;
+  const bool reuse = (a.pv.hints & IBP_HINT_ROW_REUSE) != 0;
 
   auto present = [&](uint64_t j) -> bool {
     return j < J && lane < G && row_first + j * row_step + lane < a.n_out;
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kDecWarpsMax * 32) k_decompress(const DecodeAr
       const uint32_t* src = reinterpret_cast<const uint32_t*>(__shfl_sync(kFull, src_l, q));
       uint32_t* dst = sb + q * rowcap;
       if (a.vec) {
-        for (uint32_t c = lane; c < (pre >> 2); c += 32) cp_async16(dst + 4u * c, src + 4u * c);
+        for (uint32_t c = lane; c < (pre >> 2); c += 32) cp_row16(reuse, dst + 4u * c, src + 4u * c);
       } else {
         for (uint32_t k = lane; k < pre; k += 32) cp_async4(dst + k, src + k);
       }
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kDecWarpsMax * 32) k_decompress(const DecodeAr
       const uint32_t ntq = __shfl_sync(kFull, nt, q);
       uint32_t* dst = sb + q * rowcap;
       if (a.vec) {
-        for (uint32_t c = (pre >> 2) + lane; c < ((ntq + 3u) >> 2); c += 32) cp_async16(dst + 4u * c, src + 4u * c);
+        for (uint32_t c = (pre >> 2) + lane; c < ((ntq + 3u) >> 2); c += 32) cp_row16(reuse, dst + 4u * c, src + 4u * c);
       } else {
         for (uint32_t k = pre + lane; k < ntq; k += 32) cp_async4(dst + k, src + k);
       }

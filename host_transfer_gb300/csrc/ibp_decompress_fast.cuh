@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
     }
     __syncthreads();
   }
+  const bool reuse = (a.pv.hints & IBP_HINT_ROW_REUSE) != 0;
   const uint32_t pre = a.pre;          // multiple of 4, <= W
   const uint32_t pre_ch = pre >> 2;    // prefix chunks per row
   const uint32_t n_rows32 = static_cast<uint32_t>(a.n_rows);  // < 2^31 (checked by the launcher)
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
 #pragma unroll
         for (uint32_t b = 0; b < CB; ++b) {
           const uint32_t c = lane + 32u * b;
-          if (c < pre_ch) cp_async16(dst + 4u * c, src + 4u * c);
+          if (c < pre_ch) cp_row16(reuse, dst + 4u * c, src + 4u * c);
         }
       }
     }
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
       const uint32_t ntq = __shfl_sync(kAll, nt, q);
       const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
       uint32_t* dst = sb + q * W;
-      for (uint32_t c = pre_ch + lane; c < ((ntq + 3u) >> 2); c += 32) cp_async16(dst + 4u * c, src + 4u * c);
+      for (uint32_t c = pre_ch + lane; c < ((ntq + 3u) >> 2); c += 32) cp_row16(reuse, dst + 4u * c, src + 4u * c);
     }
   };
 

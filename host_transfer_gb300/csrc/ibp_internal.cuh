@@ -54,6 +54,7 @@ struct PlanView {
   const uint32_t* eplanes;
   uint32_t* status;
   uint32_t p_min, p_scale, npl;
+  uint32_t hints;  // IBP_HINT_* bits set by ibp_plan_set_hints
   // Uniform plans (every word position has the same Mask/Bitval): scalars.
   uint32_t u_mask, u_bm, u_p, u_keep;
   uint32_t u_rmask[kMaxRuns];
@@ -155,9 +156,29 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
+// 16-byte asynchronous global -> shared copy, cached in L2 only (streaming
+// rows: each is read once per call).
 __device__ __forceinline__ void cp_async16(uint32_t* smem_dst, const void* gsrc) {
   uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+
+// The same copy, also allocating in L1: a row requested again by the same SM
+// (repeated ids, e.g. Zipf-distributed lookups) is then served from L1
+// instead of crossing the host link again.  Mapped host memory is not kept
+// in L2, so L1 is the only on-chip place a repeat can hit.
+__device__ __forceinline__ void cp_async16_l1(uint32_t* smem_dst, const void* gsrc) {
+  uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+
+// Row copy of the decoders: L1-allocating when the plan carries
+// IBP_HINT_ROW_REUSE (warp-uniform branch).
+__device__ __forceinline__ void cp_row16(bool l1, uint32_t* smem_dst, const void* gsrc) {
+  if (l1)
+    cp_async16_l1(smem_dst, gsrc);
+  else
+    cp_async16(smem_dst, gsrc);
 }
 
 __device__ __forceinline__ void cp_async4(uint32_t* smem_dst, const void* gsrc) {

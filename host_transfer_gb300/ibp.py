@@ -35,6 +35,8 @@ IBP_ECORRUPT = 4
 IBP_ERANGE = 5
 IBP_ETIMEOUT = 6
 
+IBP_HINT_ROW_REUSE = 1
+
 _lib = None
 
 
@@ -76,6 +78,7 @@ def load():
         "ibp_plan_destroy": ([vp], i32),
         "ibp_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], i32),
         "ibp_plan_get_mask": ([vp, vp, vp], i32),
+        "ibp_plan_set_hints": ([vp, u32], i32),
         "ibp_compress": ([vp, vp, vp, u64, vp, vp, vp], i32),
         "ibp_gather_decompress": ([vp, vp, u64, vp, vp, u64, vp, vp], i32),
         "ibp_decompress_contig": ([vp, vp, u64, vp, u64, u64, vp, vp], i32),
@@ -199,6 +202,10 @@ class Plan:
         inf = PlanInfo()
         _check(lib.ibp_plan_get_info(self.handle, ctypes.byref(inf)), "ibp_plan_get_info")
         return {k: getattr(inf, k) for k, _ in PlanInfo._fields_}
+
+    def set_hints(self, hints: int):
+        """IBP_HINT_* access hints for later decompress calls (0 = default)."""
+        _check(load().ibp_plan_set_hints(self.handle, int(hints)), "ibp_plan_set_hints")
 
     def mask_bitval(self):
         lib = load()

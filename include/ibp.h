@@ -63,6 +63,9 @@ extern "C" {
 #define IBP_MAX_W 8192u
 #define IBP_NOALLOC_MAX_W 4096u
 
+/* Hints for ibp_plan_set_hints (bit flags). */
+#define IBP_HINT_ROW_REUSE 1u /* calls request the same rows repeatedly (skewed ids) */
+
 typedef enum ibp_status {
   IBP_OK = 0,       /* success */
   IBP_EINVAL = 1,   /* invalid argument (size, pointer kind, T, ...) */
@@ -170,6 +173,21 @@ int ibp_plan_destroy(ibp_plan* plan);
 
 /* Fills *out with the plan's shape and table statistics. */
 int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out);
+
+/*
+ * Access hints for the decompress calls made with this plan (a bit set of
+ * IBP_HINT_*; 0 restores the default).  They change speed, never results.
+ *
+ * IBP_HINT_ROW_REUSE: the row ids of a call repeat a lot (skewed lookups such
+ * as Zipf-distributed embedding ids).  Row copies then also allocate in the
+ * SM's L1, so a repeat is served on chip instead of being fetched again over
+ * the host link (mapped host memory is not kept in L2).  For ids without
+ * repeats it costs a few percent, so it is off by default.
+ *
+ * Takes effect for calls issued after it returns; not synchronised with
+ * calls in flight.  Errors: IBP_EINVAL (NULL plan, unknown bits).
+ */
+int ibp_plan_set_hints(ibp_plan* plan, uint32_t hints);
 
 /* The plan's Mask and Bitval (W words each) copied to host memory `mask` and
  * `bitval` (either may be NULL).  Synchronous. */

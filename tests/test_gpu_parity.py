@@ -399,3 +399,24 @@ def test_per_word_plans_fast_table_modes(W, kind):
     assert plan.info["uniform"] == 0
     if kind == "up_to_4_runs":
         assert plan.info["max_runs"] == 4
+
+
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_row_reuse_hint_same_results(where):
+    """IBP_HINT_ROW_REUSE changes the cache policy of the row copies only."""
+    c = workloads.CONFIGS["tiny"]
+    rows = workloads.make_table("tiny")
+    g = gpu_codec(rows, rows[:256], c["T"], where)
+    rng = np.random.default_rng(21)
+    hot = rng.integers(0, len(rows), 5)
+    ids = np.where(rng.random(6000) < 0.7, hot[rng.integers(0, 5, 6000)], rng.integers(0, len(rows), 6000))
+    ids_t = torch.from_numpy(ids.astype(np.int64)).cuda()
+    bm_t = on_device(g["bitmask"])
+    plain = ibp.ibp_gather_decompress(g["plan"], g["slots_t"], bm_t, ids_t)
+    g["plan"].set_hints(ibp.IBP_HINT_ROW_REUSE)
+    hinted = ibp.ibp_gather_decompress(g["plan"], g["slots_t"], bm_t, ids_t)
+    torch.cuda.synchronize()
+    assert torch.equal(plain, hinted)
+    assert np.array_equal(words_np(hinted), rows[ids])
+    with pytest.raises(ibp.IbpError):
+        g["plan"].set_hints(2)
