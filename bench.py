@@ -162,14 +162,25 @@ def measured_peaks() -> dict:
         return {}
 
 
+KERNEL_SOURCES = ["ibp_decompress_fast.cuh", "ibp_decompress_fast_u.cu", "ibp_decompress_fast_t.cu",
+                  "ibp_decompress.cu", "ibp_internal.cuh"]
+
+
+def kernel_sources_sha() -> str:
+    """sha256 over the sources of the decompress kernels."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "host_transfer_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def kernel_traffic(kind: str) -> float | None:
     """DRAM bytes per launch from the committed ncu summary, when it was taken
-    on the current kernel source (else None)."""
+    on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
-    src = os.path.join(ROOT, "host_transfer_gb300", "csrc", "ibp_decompress.cu")
     try:
         rec = json.load(open(path))
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = kernel_sources_sha()
     except (OSError, ValueError):
         return None
     ent = rec.get(kind)
