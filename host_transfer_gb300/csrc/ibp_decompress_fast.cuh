@@ -31,6 +31,8 @@
 namespace ibp {
 
 constexpr int kFastWarps = 8;
+constexpr int kFastStages = 3;               // shared-memory stages per warp (D >= 3)
+constexpr uint32_t kFastGroupWords = 1024;   // rows per group G = this / W (at least 1)
 constexpr uint32_t kAll = 0xFFFFFFFFu;
 
 // Words of a per-word table entry in shared memory: {run masks, packed run
@@ -51,7 +53,7 @@ struct TabShape {
 template <int SC>
 struct FastShape {
   static constexpr uint32_t W = 32u * SC;
-  static constexpr uint32_t G = SC >= 32 ? 1u : 32u / SC;  // rows per group: G * W <= 1024 words
+  static constexpr uint32_t G = kFastGroupWords / W >= 1 ? kFastGroupWords / W : 1u;  // rows per group
   static constexpr uint32_t STAGE = G * W + 32u;           // words per stage
   static constexpr uint32_t CH = W / 4;                    // 16-byte chunks per row
   static constexpr uint32_t CB = (CH + 31) / 32;           // chunk blocks of 32 per row
@@ -69,7 +71,8 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   const uint32_t nw_cta = blockDim.x >> 5;
   uint32_t* const tab = smem;             // [W][EW] per-word entries (TAB)
   uint32_t* const epl = smem + T::ENT;    // [SC][NPL] e-planes (TAB, NPL > 0)
-  uint32_t* const stages = smem + T::WORDS + warp * 3u * STAGE;
+  constexpr int D = kFastStages;
+  uint32_t* const stages = smem + T::WORDS + warp * static_cast<uint32_t>(D) * STAGE;
   const uint32_t lt = lanemask_lt();
   const uint32_t lanebit = 1u << lane;
 
@@ -281,48 +284,62 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
     }
   };
 
-  // Pipeline: commit order per iteration is prefix(j+2), rest(j+1); see
-  // k_decompress for the wait arithmetic.
+  // Pipeline over D stages: at iteration j, st[k] holds group j + k.  Per
+  // iteration: load the ids of group j+D, issue the prefix of group j+D-1,
+  // read the kinds of group j+1 from its landed headers and issue its rest,
+  // decode group j.  cp.async groups are committed in the order prefix(j+D-1),
+  // rest(j+1); the prologue commits an empty group after each of its first
+  // D-2 prefixes so that every iteration sees the same order.  Then the
+  // prefix of j+1 is complete once at most 2D-4 groups are pending (rest(j+D-3)
+  // .. prefix(j+D-1)), and the rest of j once at most 2 are (prefix(j+D-1),
+  // rest(j+1)).
   uint64_t rb0 = gw * G;  // first output row of group j
-  int32_t id0 = load_id(0, rb0), id1 = load_id(1, rb0 + row_step), id2 = load_id(2, rb0 + 2 * row_step);
-  uint32_t* st0 = stages;
-  uint32_t* st1 = stages + STAGE;
-  uint32_t* st2 = stages + 2 * STAGE;
-  uint32_t bm0 = 0, bm1 = 0;
-  issue_prefix(0, st0, id0, bm0);
-  cp_commit();
-  issue_prefix(1, st1, id1, bm1);
-  cp_commit();
-  cp_wait<1>();
+  int32_t idr[D + 1];     // ids of groups j .. j+D
+  uint32_t bmr[D];        // bitmask words of groups j .. j+D-1
+  uint32_t* st[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) {
+    st[i] = stages + i * STAGE;
+    bmr[i] = 0;
+    idr[i] = load_id(i, rb0 + i * row_step);
+  }
+#pragma unroll
+  for (int i = 0; i < D - 1; ++i) {
+    issue_prefix(i, st[i], idr[i], bmr[i]);
+    cp_commit();
+    if (i < D - 2) cp_commit();
+  }
+  cp_wait<2 * D - 4>();
   __syncwarp();
   uint32_t kind0, nt0;
-  row_info(st0, id0, bm0, kind0, nt0);
-  issue_rest(0, st0, id0, kind0, nt0);
+  row_info(st[0], idr[0], bmr[0], kind0, nt0);
+  issue_rest(0, st[0], idr[0], kind0, nt0);
   cp_commit();
 
   for (uint64_t j = 0; j < J; ++j, rb0 += row_step) {
-    const int32_t id3 = load_id(j + 3, rb0 + 3 * row_step);
-    uint32_t bm2 = 0;
-    issue_prefix(j + 2, st2, id2, bm2);
+    idr[D] = load_id(j + D, rb0 + D * row_step);
+    issue_prefix(j + D - 1, st[D - 1], idr[D - 1], bmr[D - 1]);
     cp_commit();
-    cp_wait<2>();
+    cp_wait<2 * D - 4>();
     __syncwarp();
     uint32_t kind1, nt1;
-    row_info(st1, id1, bm1, kind1, nt1);
-    issue_rest(j + 1, st1, id1, kind1, nt1);
+    row_info(st[1], idr[1], bmr[1], kind1, nt1);
+    issue_rest(j + 1, st[1], idr[1], kind1, nt1);
     cp_commit();
     cp_wait<2>();
     __syncwarp();
-    decode_group(st0, rb0, kind0);
+    decode_group(st[0], rb0, kind0);
     __syncwarp();
-    id1 = id2;
-    id2 = id3;
-    bm1 = bm2;
     kind0 = kind1;
-    uint32_t* const t = st0;
-    st0 = st1;
-    st1 = st2;
-    st2 = t;
+    uint32_t* const t = st[0];
+#pragma unroll
+    for (int i = 0; i < D - 1; ++i) st[i] = st[i + 1];
+    st[D - 1] = t;
+#pragma unroll
+    for (int i = 0; i < D; ++i) idr[i] = idr[i + 1];
+#pragma unroll
+    for (int i = 0; i < D - 1; ++i) bmr[i] = bmr[i + 1];
+    bmr[D - 1] = 0;
   }
   cp_wait<0>();
 }
@@ -331,7 +348,7 @@ template <int R, int SC, int NPL, bool TAB>
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   using F = FastShape<SC>;
   using T = TabShape<SC, R, NPL, TAB>;
-  const size_t per_warp = 4ull * 3ull * F::STAGE;
+  const size_t per_warp = 4ull * kFastStages * F::STAGE;
   const size_t fixed = 4ull * T::WORDS;
   size_t warps = (220ull * 1024 - fixed) / per_warp;
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
