@@ -276,7 +276,8 @@ int ibp_compress(const ibp_plan* plan, const uint32_t* rows, uint32_t* slots, ui
 
 static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
                              const uint32_t* bitmask, const int64_t* ids, uint64_t first,
-                             uint64_t n_out, uint32_t* out, void* stream) {
+                             uint64_t n_out, uint32_t* out, void* stream,
+                             const uint64_t* offsets = nullptr) {
   const uint64_t W = plan->W;
   if (n_rows > (~0ull) / (4 * W) || n_out > (~0ull) / (4 * W)) return IBP_EINVAL;
   DeviceGuard g(plan->device);
@@ -286,7 +287,10 @@ static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64
       resolve_ptr(out, plan->device, &dout))
     return IBP_EINVAL;
   if (ids && resolve_ptr(ids, plan->device, &dids)) return IBP_EINVAL;
+  const void* doff = nullptr;
+  if (offsets && resolve_ptr(offsets, plan->device, &doff)) return IBP_EINVAL;
   DecodeArgs a;
+  a.offsets = static_cast<const uint64_t*>(doff);
   a.pv = plan->view;
   a.slots = static_cast<const uint32_t*>(dsl);
   a.bitmask = static_cast<const uint32_t*>(dbm);
@@ -303,6 +307,10 @@ static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64
   if (a.pre > W) a.pre = static_cast<uint32_t>(W);
   uint32_t G = 1152u / static_cast<uint32_t>(W + 4);
   a.G = G < 1 ? 1 : (G > 32 ? 32 : G);
+  if (a.offsets) {  // the packed layout is decoded by the specialised kernel only
+    if (!fast_decompress_applies(plan, a)) return IBP_EINVAL;
+    return launch_decompress_fast(plan, a, static_cast<cudaStream_t>(stream));
+  }
   return launch_decompress(plan, a, static_cast<cudaStream_t>(stream));
 }
 
@@ -325,6 +333,64 @@ int ibp_decompress_contig(const ibp_plan* plan, const uint32_t* slots, uint64_t 
   if (!slots || !bitmask || !out) return IBP_EINVAL;
   if (first_row >= n_rows || n > n_rows - first_row) return IBP_EINVAL;
   return decompress_common(plan, slots, n_rows, bitmask, nullptr, first_row, n, out, stream);
+}
+
+int ibp_packed_offsets(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                       const uint32_t* bitmask, uint64_t* offsets, void* stream) {
+  g_detail[0] = 0;
+  if (!plan || !offsets || plan->W % 4u) return IBP_EINVAL;
+  if (n_rows == 0) {
+    DeviceGuard g(plan->device);
+    if (!g.ok) return IBP_ECUDA;
+    cudaError_t e = cudaMemsetAsync(offsets, 0, sizeof(uint64_t), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+      set_cuda_error(e, "cudaMemsetAsync");
+      cudaGetLastError();
+      return IBP_ECUDA;
+    }
+    return IBP_OK;
+  }
+  if (!slots || !bitmask || n_rows > (~0ull) / (4ull * plan->W)) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void *ds, *db, *dof;
+  if (resolve_ptr(slots, plan->device, &ds) || resolve_ptr(bitmask, plan->device, &db) ||
+      resolve_ptr(offsets, plan->device, &dof))
+    return IBP_EINVAL;
+  return launch_packed_offsets(plan, static_cast<const uint32_t*>(ds), n_rows,
+                               static_cast<const uint32_t*>(db),
+                               const_cast<uint64_t*>(static_cast<const uint64_t*>(dof)),
+                               static_cast<cudaStream_t>(stream));
+}
+
+int ibp_pack(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows, const uint64_t* offsets,
+             uint32_t* packed, void* stream) {
+  g_detail[0] = 0;
+  if (!plan || plan->W % 4u) return IBP_EINVAL;
+  if (n_rows == 0) return IBP_OK;
+  if (!slots || !offsets || !packed || n_rows > (~0ull) / (4ull * plan->W)) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void *ds, *dof, *dp;
+  if (resolve_ptr(slots, plan->device, &ds) || resolve_ptr(offsets, plan->device, &dof) ||
+      resolve_ptr(packed, plan->device, &dp))
+    return IBP_EINVAL;
+  if (!aligned16(ds) || !aligned16(dp)) return IBP_EINVAL;
+  return launch_pack(static_cast<const uint32_t*>(ds), n_rows, plan->W,
+                     static_cast<const uint64_t*>(dof),
+                     const_cast<uint32_t*>(static_cast<const uint32_t*>(dp)), plan->device,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int ibp_gather_decompress_packed(const ibp_plan* plan, const uint32_t* packed,
+                                 const uint64_t* offsets, uint64_t n_rows,
+                                 const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
+                                 uint32_t* out, void* stream) {
+  g_detail[0] = 0;
+  if (!plan) return IBP_EINVAL;
+  if (n_ids == 0) return IBP_OK;
+  if (!packed || !offsets || !bitmask || !row_ids || !out || n_rows == 0) return IBP_EINVAL;
+  return decompress_common(plan, packed, n_rows, bitmask, row_ids, 0, n_ids, out, stream, offsets);
 }
 
 int ibp_get_status(const ibp_plan* plan, void* stream) {

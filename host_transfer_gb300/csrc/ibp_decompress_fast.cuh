@@ -59,7 +59,11 @@ struct FastShape {
   static constexpr uint32_t CB = (CH + 31) / 32;           // chunk blocks of 32 per row
 };
 
-template <int R, int SC, int NPL, bool TAB>
+// PK = false: row r of the table is slots[r * W ..]; PK = true: the packed
+// layout, row r is slots[offsets[r] .. offsets[r + 1]) (its stored words
+// rounded up to 16 bytes), and a row whose stream would reach past that
+// extent is corrupt.
+template <int R, int SC, int NPL, bool TAB, bool PK>
 __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const DecodeArgs a) {
   using F = FastShape<SC>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -126,15 +130,41 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
     return (id >= 0 && static_cast<uint64_t>(id) < n_rows32) ? static_cast<int32_t>(id) : kBadId;
   };
 
+  // Word offset of a row in the slots (PK: in the packed buffer) and the
+  // number of words it occupies there.
+  struct RowPos {
+    uint64_t off;
+    uint32_t ext;
+  };
+  auto row_pos = [&](int32_t id) -> RowPos {
+    if constexpr (PK) {
+      if (id < 0) return {0, 0};
+      const uint64_t lo = a.offsets[id], hi = a.offsets[id + 1];
+      const uint64_t ext = hi > lo ? hi - lo : 0;
+      return {lo, static_cast<uint32_t>(ext < W ? ext : W)};
+    } else {
+      return {static_cast<uint64_t>(id >= 0 ? id : 0) * W, W};
+    }
+  };
+
   // Prefix of group j: lane i copies chunk i (+32 ...) of every row.
-  auto issue_prefix = [&](uint64_t j, uint32_t* sb, int32_t id, uint32_t& bmw) {
+  auto issue_prefix = [&](uint64_t j, uint32_t* sb, int32_t id, RowPos rp, uint32_t& bmw) {
     if (id >= 0) bmw = ld_u32(a.bitmask + (static_cast<uint32_t>(id) >> 5));
     if (j >= J) return;
 #pragma unroll
     for (uint32_t q = 0; q < G; ++q) {
       const int32_t idq = __shfl_sync(kAll, id, q);
-      if (idq >= 0) {
-        const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
+      uint64_t offq;
+      if constexpr (PK)
+        offq = __shfl_sync(kAll, static_cast<unsigned long long>(rp.off), q);
+      else
+        offq = static_cast<uint64_t>(idq) * W;
+      // PK: a row shorter than the prefix is corrupt (row_info says so) and
+      // is not read
+      bool ok = idq >= 0;
+      if constexpr (PK) ok = ok && __shfl_sync(kAll, rp.ext, q) >= pre;
+      if (ok) {
+        const uint32_t* src = a.slots + offq;
         uint32_t* dst = sb + q * W;
 #pragma unroll
         for (uint32_t b = 0; b < CB; ++b) {
@@ -146,7 +176,8 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   };
 
   // Kind and stream length of lane q's row of group j (headers in stage).
-  auto row_info = [&](const uint32_t* sb, int32_t id, uint32_t bmw, uint32_t& kind, uint32_t& nt) {
+  auto row_info = [&](const uint32_t* sb, int32_t id, RowPos rp, uint32_t bmw, uint32_t& kind,
+                      uint32_t& nt) {
     kind = kNone;
     nt = 0;
     if (id == kNoRow) return;
@@ -155,8 +186,12 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
       return;
     }
     if (!((bmw >> (static_cast<uint32_t>(id) & 31u)) & 1u)) {
-      kind = kRaw;
-      nt = W;
+      kind = (PK && rp.ext < W) ? kCorrupt : kRaw;
+      nt = kind == kRaw ? W : 0u;
+      return;
+    }
+    if (PK && rp.ext < pre) {
+      kind = kCorrupt;
       return;
     }
     const uint32_t* hb = sb + lane * W;
@@ -183,7 +218,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
       for (uint32_t s = 0; s < SC; ++s) count(hb[s], s);
     }
     const uint32_t Lw = (32u * (SC + W) - p * m - pscale * me + 31u) >> 5;
-    if (Lw >= W) {
+    if (Lw >= W || (PK && ((Lw + 3u) & ~3u) > rp.ext)) {
       kind = kCorrupt;
       return;
     }
@@ -192,14 +227,18 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   };
 
   // Rest of group j: [pre, Lw) of compressed rows, [pre, W) of raw rows.
-  auto issue_rest = [&](uint64_t j, uint32_t* sb, int32_t id, uint32_t kind, uint32_t nt) {
+  auto issue_rest = [&](uint64_t j, uint32_t* sb, int32_t id, RowPos rp, uint32_t kind, uint32_t nt) {
     if (j >= J) return;
     const bool need = (kind == kRaw || kind == kComp) && nt > pre;
     for (uint32_t mk = __ballot_sync(kAll, need); mk; mk &= mk - 1) {
       const uint32_t q = __ffs(mk) - 1;
-      const int32_t idq = __shfl_sync(kAll, id, q);
       const uint32_t ntq = __shfl_sync(kAll, nt, q);
-      const uint32_t* src = a.slots + static_cast<uint64_t>(idq) * W;
+      uint64_t offq;
+      if constexpr (PK)
+        offq = __shfl_sync(kAll, static_cast<unsigned long long>(rp.off), q);
+      else
+        offq = static_cast<uint64_t>(__shfl_sync(kAll, id, q)) * W;
+      const uint32_t* src = a.slots + offq;
       uint32_t* dst = sb + q * W;
       for (uint32_t c = pre_ch + lane; c < ((ntq + 3u) >> 2); c += 32) cp_row16(reuse, dst + 4u * c, src + 4u * c);
     }
@@ -293,38 +332,45 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   // prefix of j+1 is complete once at most 2D-4 groups are pending (rest(j+D-3)
   // .. prefix(j+D-1)), and the rest of j once at most 2 are (prefix(j+D-1),
   // rest(j+1)).
+  // PK: a group's ids are loaded one iteration before its row offsets, and
+  // its offsets one iteration before its prefix, so ids run D+1 groups ahead.
+  constexpr int IA = PK ? D + 1 : D;
   uint64_t rb0 = gw * G;  // first output row of group j
-  int32_t idr[D + 1];     // ids of groups j .. j+D
+  int32_t idr[IA + 1];    // ids of groups j .. j+IA
+  RowPos rpr[D + 1];      // row positions of groups j .. j+D (PK: loaded; else from the id)
   uint32_t bmr[D];        // bitmask words of groups j .. j+D-1
   uint32_t* st[D];
+#pragma unroll
+  for (int i = 0; i < IA; ++i) idr[i] = load_id(i, rb0 + i * row_step);
 #pragma unroll
   for (int i = 0; i < D; ++i) {
     st[i] = stages + i * STAGE;
     bmr[i] = 0;
-    idr[i] = load_id(i, rb0 + i * row_step);
+    rpr[i] = row_pos(idr[i]);
   }
 #pragma unroll
   for (int i = 0; i < D - 1; ++i) {
-    issue_prefix(i, st[i], idr[i], bmr[i]);
+    issue_prefix(i, st[i], idr[i], rpr[i], bmr[i]);
     cp_commit();
     if (i < D - 2) cp_commit();
   }
   cp_wait<2 * D - 4>();
   __syncwarp();
   uint32_t kind0, nt0;
-  row_info(st[0], idr[0], bmr[0], kind0, nt0);
-  issue_rest(0, st[0], idr[0], kind0, nt0);
+  row_info(st[0], idr[0], rpr[0], bmr[0], kind0, nt0);
+  issue_rest(0, st[0], idr[0], rpr[0], kind0, nt0);
   cp_commit();
 
   for (uint64_t j = 0; j < J; ++j, rb0 += row_step) {
-    idr[D] = load_id(j + D, rb0 + D * row_step);
-    issue_prefix(j + D - 1, st[D - 1], idr[D - 1], bmr[D - 1]);
+    idr[IA] = load_id(j + IA, rb0 + IA * row_step);
+    if constexpr (PK) rpr[D] = row_pos(idr[D]);
+    issue_prefix(j + D - 1, st[D - 1], idr[D - 1], rpr[D - 1], bmr[D - 1]);
     cp_commit();
     cp_wait<2 * D - 4>();
     __syncwarp();
     uint32_t kind1, nt1;
-    row_info(st[1], idr[1], bmr[1], kind1, nt1);
-    issue_rest(j + 1, st[1], idr[1], kind1, nt1);
+    row_info(st[1], idr[1], rpr[1], bmr[1], kind1, nt1);
+    issue_rest(j + 1, st[1], idr[1], rpr[1], kind1, nt1);
     cp_commit();
     cp_wait<2>();
     __syncwarp();
@@ -336,7 +382,10 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
     for (int i = 0; i < D - 1; ++i) st[i] = st[i + 1];
     st[D - 1] = t;
 #pragma unroll
-    for (int i = 0; i < D; ++i) idr[i] = idr[i + 1];
+    for (int i = 0; i < IA; ++i) idr[i] = idr[i + 1];
+#pragma unroll
+    for (int i = 0; i < D; ++i) rpr[i] = rpr[i + 1];
+    if constexpr (!PK) rpr[D - 1] = row_pos(idr[D - 1]);
 #pragma unroll
     for (int i = 0; i < D - 1; ++i) bmr[i] = bmr[i + 1];
     bmr[D - 1] = 0;
@@ -344,7 +393,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   cp_wait<0>();
 }
 
-template <int R, int SC, int NPL, bool TAB>
+template <int R, int SC, int NPL, bool TAB, bool PK>
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   using F = FastShape<SC>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -354,7 +403,7 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = fixed + warps * per_warp;
-  auto kern = k_decompress_fast<R, SC, NPL, TAB>;
+  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
   // for this launch shape.
   static int occ_cache[64] = {0};
@@ -380,21 +429,48 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   return check_launch("k_decompress_fast");
 }
 
-template <int R, int NPL, bool TAB>
+template <int R, int NPL, bool TAB, bool PK>
 static int launch_fast_sc(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   switch (plan->S) {
-    case 1: return launch_fast_t<R, 1, NPL, TAB>(plan, a, stream);
-    case 2: return launch_fast_t<R, 2, NPL, TAB>(plan, a, stream);
-    case 4: return launch_fast_t<R, 4, NPL, TAB>(plan, a, stream);
-    case 8: return launch_fast_t<R, 8, NPL, TAB>(plan, a, stream);
-    case 16: return launch_fast_t<R, 16, NPL, TAB>(plan, a, stream);
-    case 32: return launch_fast_t<R, 32, NPL, TAB>(plan, a, stream);
-    default: return launch_fast_t<R, 64, NPL, TAB>(plan, a, stream);
+    case 1: return launch_fast_t<R, 1, NPL, TAB, PK>(plan, a, stream);
+    case 2: return launch_fast_t<R, 2, NPL, TAB, PK>(plan, a, stream);
+    case 4: return launch_fast_t<R, 4, NPL, TAB, PK>(plan, a, stream);
+    case 8: return launch_fast_t<R, 8, NPL, TAB, PK>(plan, a, stream);
+    case 16: return launch_fast_t<R, 16, NPL, TAB, PK>(plan, a, stream);
+    case 32: return launch_fast_t<R, 32, NPL, TAB, PK>(plan, a, stream);
+    default: return launch_fast_t<R, 64, NPL, TAB, PK>(plan, a, stream);
   }
 }
 
-// Instantiated in ibp_decompress_fast_u.cu and ibp_decompress_fast_t.cu.
+template <bool PK>
+static int launch_fast_uniform_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  switch (plan->max_runs) {
+    case 1: return launch_fast_sc<1, 0, false, PK>(plan, a, stream);
+    case 2: return launch_fast_sc<2, 0, false, PK>(plan, a, stream);
+    case 3: return launch_fast_sc<3, 0, false, PK>(plan, a, stream);
+    default: return launch_fast_sc<4, 0, false, PK>(plan, a, stream);
+  }
+}
+
+template <int R, bool PK>
+static int launch_table_r(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  switch (plan->view.npl) {
+    case 0: return launch_fast_sc<R, 0, true, PK>(plan, a, stream);
+    case 1: return launch_fast_sc<R, 1, true, PK>(plan, a, stream);
+    default: return launch_fast_sc<R, 6, true, PK>(plan, a, stream);
+  }
+}
+
+template <bool PK>
+static int launch_fast_table_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  return plan->max_runs <= 2 ? launch_table_r<2, PK>(plan, a, stream) : launch_table_r<4, PK>(plan, a, stream);
+}
+
+// One translation unit each (compiled in parallel): slot layout uniform and
+// table plans, packed layout uniform and table plans.
 int launch_fast_uniform(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_table(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+int launch_fast_uniform_packed(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+int launch_fast_table_packed(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace ibp

@@ -1,17 +1,12 @@
-// ibp_decompress_fast_u.cu - uniform-plan instantiations of the specialised
-// decompress kernel (ibp_decompress_fast.cuh) and the choice between the
-// specialised kernels and the general one.
+// ibp_decompress_fast_u.cu - uniform-plan instantiations (slot layout) of the
+// specialised decompress kernel (ibp_decompress_fast.cuh), and the choice
+// between the specialised kernels and the general one.
 #include "ibp_decompress_fast.cuh"
 
 namespace ibp {
 
 int launch_fast_uniform(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  switch (plan->max_runs) {
-    case 1: return launch_fast_sc<1, 0, false>(plan, a, stream);
-    case 2: return launch_fast_sc<2, 0, false>(plan, a, stream);
-    case 3: return launch_fast_sc<3, 0, false>(plan, a, stream);
-    default: return launch_fast_sc<4, 0, false>(plan, a, stream);
-  }
+  return launch_fast_uniform_t<false>(plan, a, stream);
 }
 
 bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a) {
@@ -25,6 +20,9 @@ bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a) {
 }
 
 int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  if (a.offsets)
+    return plan->uniform ? launch_fast_uniform_packed(plan, a, stream)
+                         : launch_fast_table_packed(plan, a, stream);
   return plan->uniform ? launch_fast_uniform(plan, a, stream) : launch_fast_table(plan, a, stream);
 }
 

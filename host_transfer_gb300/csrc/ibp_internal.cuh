@@ -96,6 +96,7 @@ struct DecodeArgs {
   const uint32_t* slots;   // row 0 of the table
   const uint32_t* bitmask;
   const int64_t* ids;      // nullptr: rows first, first + 1, ...
+  const uint64_t* offsets; // packed layout: row r at slots[offsets[r] .. offsets[r+1]); else nullptr
   uint64_t first;
   uint64_t n_rows;         // rows in the table
   uint64_t n_out;          // rows to produce
@@ -112,6 +113,13 @@ int launch_decompress(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 // 2^31 rows (ibp_decompress_fast.cu).
 bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a);
 int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+
+// Packed cache layout (ibp_packed.cu): per-row stored lengths rounded up to
+// 4 words and their exclusive scan; the copy of slots into packed rows.
+int launch_packed_offsets(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                          const uint32_t* bitmask, uint64_t* offsets, cudaStream_t stream);
+int launch_pack(const uint32_t* slots, uint64_t n_rows, uint32_t W, const uint64_t* offsets,
+                uint32_t* packed, int device, cudaStream_t stream);
 
 struct CompressArgs {
   PlanView pv;

@@ -85,6 +85,9 @@ def load():
         "ibp_get_status": ([vp, vp], i32),
         "ibp_gather_raw": ([vp, u64, u32, vp, u64, vp, vp], i32),
         "ibp_row_lengths": ([vp, vp, u64, vp, vp, u64, vp, vp], i32),
+        "ibp_packed_offsets": ([vp, vp, u64, vp, vp, vp], i32),
+        "ibp_pack": ([vp, vp, u64, vp, vp, vp], i32),
+        "ibp_gather_decompress_packed": ([vp, vp, vp, u64, vp, vp, u64, vp, vp], i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -319,6 +322,49 @@ def ibp_row_lengths(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_
     with torch.cuda.device(dev):
         _check(lib.ibp_row_lengths(plan.handle, _ptr(s), n, _ptr(bitmask), _ptr(row_ids), k,
                                    _ptr(out), _stream(stream, dev)), "ibp_row_lengths")
+    return out
+
+
+def ibp_packed_offsets(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor,
+                       offsets: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Row offsets (int64 device tensor of n_rows + 1 words) of the packed cache
+    layout of these slots; offsets[-1] is the packed size in words."""
+    lib = load()
+    sp, n, W = _word_rows(slots)
+    if offsets is None:
+        offsets = torch.empty(n + 1, dtype=torch.int64, device=torch.device("cuda", plan.device))
+    _check(lib.ibp_packed_offsets(plan.handle, sp, n, _ptr(bitmask), _ptr(offsets),
+                                  _stream(stream, plan.device)), "ibp_packed_offsets")
+    return offsets
+
+
+def ibp_pack(plan: Plan, slots: torch.Tensor, offsets: torch.Tensor, packed: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """Packed copy of the slots (int32 device tensor of offsets[-1] words).
+    Allocating it reads offsets[-1] back to the host (a synchronisation)."""
+    lib = load()
+    sp, n, W = _word_rows(slots)
+    if packed is None:
+        total = int(offsets[-1].item())
+        packed = torch.empty(max(total, 4), dtype=torch.int32, device=torch.device("cuda", plan.device))
+    _check(lib.ibp_pack(plan.handle, sp, n, _ptr(offsets), _ptr(packed), _stream(stream, plan.device)),
+           "ibp_pack")
+    return packed
+
+
+def ibp_gather_decompress_packed(plan: Plan, packed: torch.Tensor, offsets: torch.Tensor,
+                                 bitmask: torch.Tensor, row_ids: torch.Tensor,
+                                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    lib = load()
+    if row_ids.dtype != torch.int64 or not row_ids.is_contiguous():
+        raise ValueError("row_ids must be a contiguous int64 tensor")
+    n_rows = offsets.numel() - 1
+    k = row_ids.numel()
+    if out is None:
+        out = torch.empty((k, plan.W), dtype=torch.int32, device=torch.device("cuda", plan.device))
+    _check(lib.ibp_gather_decompress_packed(plan.handle, _ptr(packed), _ptr(offsets), n_rows,
+                                            _ptr(bitmask), _ptr(row_ids), k, _ptr(out),
+                                            _stream(stream, plan.device)), "ibp_gather_decompress_packed")
     return out
 
 

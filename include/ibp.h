@@ -251,6 +251,41 @@ int ibp_decompress_contig(const ibp_plan* plan, const uint32_t* slots, uint64_t 
                           uint32_t* out, void* stream);
 
 /*
+ * Packed cache layout - « Intégration au système », cache compression:
+ * compressing the tensors held in a GPU software cache raises the cache's
+ * effective capacity.  Fixed-size slots save no space, so a cache keeps each
+ * row's stored words only (Lw for a compressed row, W for a raw one), rounded
+ * up to 4 words so that rows start on 16-byte boundaries, back to back.
+ * offsets[r] is the word where row r starts and offsets[n_rows] the total
+ * number of words.  Requires W % 4 == 0.
+ *
+ * ibp_packed_offsets: fills offsets (device-accessible, n_rows + 1 uint64)
+ *   from the rows' headers in `slots` (as for ibp_gather_decompress).  Uses
+ *   8 bytes per 4096 rows of scratch from cudaMallocAsync, freed in stream
+ *   order.  Errors: IBP_EINVAL, IBP_ENOMEM, IBP_ECUDA.
+ * ibp_pack: copies each row's stored words from `slots` (device-accessible,
+ *   e.g. pinned host memory: filling an HBM cache) to `packed`
+ *   (device-accessible, offsets[n_rows] words, 16-byte aligned) at
+ *   offsets[r].  `offsets` must come from ibp_packed_offsets for these slots.
+ * ibp_gather_decompress_packed: ibp_gather_decompress reading the packed
+ *   layout.  A row whose headers announce more words than its packed extent,
+ *   or a raw row whose extent is not W, records IBP_ECORRUPT and gives a zero
+ *   row.  Needs the specialised decoder's plan shape (W = 32 * 2^k <= 2048,
+ *   at most four runs of kept bits per word, W <= 1024 for per-word Masks,
+ *   16-byte aligned packed buffer and output, fewer than 2^31 rows);
+ *   IBP_EINVAL otherwise.
+ * All three are asynchronous on `stream`.
+ */
+int ibp_packed_offsets(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                       const uint32_t* bitmask, uint64_t* offsets, void* stream);
+int ibp_pack(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows, const uint64_t* offsets,
+             uint32_t* packed, void* stream);
+int ibp_gather_decompress_packed(const ibp_plan* plan, const uint32_t* packed,
+                                 const uint64_t* offsets, uint64_t n_rows,
+                                 const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
+                                 uint32_t* out, void* stream);
+
+/*
  * Synchronises `stream`, returns the first data error recorded by the plan's
  * kernels since the last call (IBP_OK if none) and clears it.  The status
  * word is shared by every call made with this plan, on any stream.

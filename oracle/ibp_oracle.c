@@ -176,6 +176,23 @@ int ibp_ref_compress(const uint32_t* rows, uint64_t n_rows, uint32_t W,
   return REF_OK;
 }
 
+/* Words a reader fetches for each row (Lw when the row is stored compressed,
+ * W when it is stored raw): the per-row sizes of a packed layout. */
+int ibp_ref_row_words(const uint32_t* rows, uint64_t n_rows, uint32_t W,
+                      const uint32_t* mask, const uint32_t* bitval, uint32_t* words) {
+  if (W == 0) return REF_EINVAL;
+  int64_t n = (int64_t)n_rows;
+#pragma omp parallel for num_threads(g_threads) schedule(static)
+  for (int64_t r = 0; r < n; ++r) {
+    uint32_t* tmp = (uint32_t*)malloc((size_t)W * sizeof(uint32_t));
+    uint64_t used = 0;
+    compress_one(rows + (uint64_t)r * W, W, mask, bitval, tmp, &used);
+    free(tmp);
+    words[r] = (uint32_t)used;
+  }
+  return REF_OK;
+}
+
 /* Compress only the rows listed in ids (each a row of `rows`); slot i and bit
  * i of out_bits describe row ids[i].  Used to check sampled rows of a table
  * too large to run through the bit-by-bit code whole. */

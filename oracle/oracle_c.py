@@ -49,6 +49,7 @@ def _load():
                                           u32p, ctypes.POINTER(ctypes.c_uint8)]
     lib.ibp_ref_decompress.argtypes = [u32p, u64, ctypes.c_uint32, u32p, u32p, u32p, i64p, u64,
                                        u32p, ctypes.POINTER(ctypes.c_int)]
+    lib.ibp_ref_row_words.argtypes = [u32p, u64, ctypes.c_uint32, u32p, u32p, u32p]
     lib.ibp_ref_decode_slots.argtypes = [u32p, ctypes.POINTER(ctypes.c_uint8), u64,
                                          ctypes.c_uint32, u32p, u32p, u32p,
                                          ctypes.POINTER(ctypes.c_int)]
@@ -101,6 +102,18 @@ def compress(rows: np.ndarray, mask: np.ndarray, bitval: np.ndarray):
                               _p(bitmask, ctypes.c_uint32), ctypes.byref(stored))
     assert st == 0, st
     return slots, bitmask, int(stored.value)
+
+
+def row_words(rows: np.ndarray, mask: np.ndarray, bitval: np.ndarray) -> np.ndarray:
+    """Per row: Lw if stored compressed, else W."""
+    lib = _load()
+    rows = _u32(rows)
+    n, W = rows.shape
+    out = np.empty(n, np.uint32)
+    st = lib.ibp_ref_row_words(_p(rows, ctypes.c_uint32), n, W, _p(_u32(mask), ctypes.c_uint32),
+                               _p(_u32(bitval), ctypes.c_uint32), _p(out, ctypes.c_uint32))
+    assert st == 0, st
+    return out
 
 
 def compress_some(rows: np.ndarray, ids: np.ndarray, mask: np.ndarray, bitval: np.ndarray):

@@ -403,3 +403,19 @@ def test_out_of_range_and_corrupt_slots():
     st, out = C.decompress(s2, bm2, np.array([0]), m2, b2)
     assert st == R.ECORRUPT and not out.any()
     assert R.decode_row(s2[0].tolist(), True, m2.tolist(), b2.tolist())[0] == R.ECORRUPT
+
+
+def test_row_words_sum_to_stored_words():
+    """Per-row stored words add up to the total the compress reports, and equal
+    W exactly for the rows stored raw."""
+    rng = np.random.default_rng(40)
+    rows = _float_rows(rng, 300, 96)
+    rows[::5] = rng.integers(0, 2**32, (60, 96), dtype=np.uint64).astype(np.uint32)
+    _, m, b = C.preprocess(rows, 0.9)
+    slots, bitmask, stored = C.compress(rows, m, b)
+    words = C.row_words(rows, m, b)
+    assert int(words.sum()) == stored
+    bits = (bitmask[np.arange(300) >> 5] >> (np.arange(300) & 31).astype(np.uint32)) & 1
+    assert np.all(words[bits == 0] == 96) and np.all(words[bits == 1] < 96)
+    for r in (0, 1, 7):
+        assert words[r] == R.compress_row(rows[r].tolist(), m.tolist(), b.tolist())[2]
