@@ -1,6 +1,8 @@
 // ibp_api.cu - the C ABI of libibp: argument checks, pointer resolution,
 // plan lifetime, status word.  Kernels live in the other .cu files.
 #include <cuda_runtime.h>
+
+#include <vector>
 #include <stdio.h>
 #include <string.h>
 
@@ -208,6 +210,17 @@ int ibp_plan_destroy(ibp_plan* plan) {
   return IBP_OK;
 }
 
+// Words a decompress call fetches from every row before it reads the row's
+// headers: the shortest stream the plan allows (in whole 16-byte chunks on the
+// vector path), or the longer prefix set by ibp_plan_tune_prefix /
+// ibp_plan_set_prefix (slot layout only), never more than W.
+static uint32_t prefix_words(const ibp_plan* plan, bool vec, bool packed = false) {
+  const uint32_t W = plan->W;
+  uint32_t pre = vec ? ((plan->lmin + 3u) / 4u) * 4u : plan->lmin;
+  if (!packed && plan->prefix > pre) pre = vec ? ((plan->prefix + 3u) / 4u) * 4u : plan->prefix;
+  return pre < W ? pre : W;
+}
+
 int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out) {
   if (!plan || !out) return IBP_EINVAL;
   out->W = plan->W;
@@ -218,12 +231,77 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out) {
   out->max_kept_bits = plan->max_kept;
   out->metadata_bytes = plan->d_bytes;
   out->device = plan->device;
+  out->prefix_words = prefix_words(plan, true);
   return IBP_OK;
 }
 
 int ibp_plan_set_hints(ibp_plan* plan, uint32_t hints) {
   if (!plan || (hints & ~IBP_HINT_ROW_REUSE)) return IBP_EINVAL;
   plan->view.hints = hints;
+  return IBP_OK;
+}
+
+int ibp_plan_set_prefix(ibp_plan* plan, uint32_t words) {
+  if (!plan) return IBP_EINVAL;
+  plan->prefix = words < plan->W ? words : plan->W;
+  return IBP_OK;
+}
+
+int ibp_plan_tune_prefix(ibp_plan* plan, const uint32_t* slots, uint64_t n_rows, const uint32_t* bitmask,
+                         uint64_t max_sample, uint32_t* prefix_words_out, void* stream) {
+  g_detail[0] = 0;
+  if (!plan || !slots || !bitmask || n_rows == 0) return IBP_EINVAL;
+  const uint64_t W = plan->W;
+  if (n_rows > (~0ull) / (4 * W)) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void *dsl, *dbm;
+  if (resolve_ptr(slots, plan->device, &dsl) || resolve_ptr(bitmask, plan->device, &dbm)) return IBP_EINVAL;
+  const uint64_t n_sample = n_rows < (max_sample ? max_sample : 65536ull) ? n_rows : (max_sample ? max_sample : 65536ull);
+  const uint32_t nb = static_cast<uint32_t>((W + 3) / 4 + 1);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* d_hist = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_hist), 4ull * nb, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return IBP_ENOMEM;
+  }
+  std::vector<uint32_t> hist(nb, 0);
+  e = cudaMemsetAsync(d_hist, 0, 4ull * nb, st);
+  int rc = e == cudaSuccess ? IBP_OK : IBP_ECUDA;
+  if (rc == IBP_OK)
+    rc = launch_length_hist(plan, static_cast<const uint32_t*>(dsl), n_rows, static_cast<const uint32_t*>(dbm),
+                            n_sample, d_hist, st);
+  if (rc == IBP_OK) {
+    e = cudaMemcpyAsync(hist.data(), d_hist, 4ull * nb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+      set_cuda_error(e, "ibp_plan_tune_prefix");
+      rc = IBP_ECUDA;
+    }
+  }
+  cudaFreeAsync(d_hist, st);
+  if (rc != IBP_OK) {
+    cudaGetLastError();
+    return rc;
+  }
+  // Chunks fetched per row with a prefix of P chunks: max(P, c) for a row of
+  // c chunks, plus kRefetch for each row that needs a second, dependent fetch
+  // (c > P).  Take the P with the smallest total, the shortest on ties.
+  constexpr uint64_t kRefetch = 8;
+  const uint32_t pmin = (plan->lmin + 3u) / 4u;
+  uint32_t best_p = pmin;
+  uint64_t best = ~0ull;
+  for (uint32_t P = pmin; P < nb; ++P) {
+    uint64_t cost = 0;
+    for (uint32_t c = 0; c < nb; ++c) cost += hist[c] * (c > P ? c + kRefetch : P);
+    if (cost < best) {
+      best = cost;
+      best_p = P;
+    }
+  }
+  plan->prefix = static_cast<uint32_t>(4ull * best_p < W ? 4ull * best_p : W);
+  if (prefix_words_out) *prefix_words_out = prefix_words(plan, W % 4 == 0);
   return IBP_OK;
 }
 
@@ -301,10 +379,9 @@ static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64
   a.out = const_cast<uint32_t*>(static_cast<const uint32_t*>(dout));
   a.vec = (W % 4 == 0) && aligned16(a.slots) && aligned16(a.out);
   a.rowcap = static_cast<uint32_t>(((W + 31) / 32) * 32);
-  // prefix: the shortest possible stream, in whole 16-byte chunks on the
-  // vector path (never past the row: W % 4 == 0 there)
-  a.pre = a.vec ? ((plan->lmin + 3u) / 4u) * 4u : plan->lmin;
-  if (a.pre > W) a.pre = static_cast<uint32_t>(W);
+  // prefix fetched before the headers (never past the row: W % 4 == 0 on the
+  // vector path)
+  a.pre = prefix_words(plan, a.vec != 0, offsets != nullptr);
   uint32_t G = 1152u / static_cast<uint32_t>(W + 4);
   a.G = G < 1 ? 1 : (G > 32 ? 32 : G);
   if (a.offsets) {  // the packed layout is decoded by the specialised kernel only

@@ -69,6 +69,7 @@ struct ibp_plan {
   uint32_t W, S;
   uint32_t uniform, max_runs, min_kept, max_kept;
   uint32_t lmin;  // min(W, words of the shortest possible compressed stream)
+  uint32_t prefix;  // words fetched before the headers (slot layout); 0 = from lmin
   void* d_block;  // single device allocation holding every table + status
   size_t d_bytes;
   ibp::PlanView view;
@@ -151,6 +152,10 @@ int build_plan_tables(ibp_plan* plan);
 int launch_row_lengths(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
                        const uint32_t* bitmask, const int64_t* ids, uint64_t n_ids,
                        uint32_t* lengths, cudaStream_t stream);
+// Histogram of the stored lengths (16-byte chunks) of n_sample evenly spaced
+// rows into hist[0 .. ceil(W/4)] (zeroed by the caller).
+int launch_length_hist(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                       const uint32_t* bitmask, uint64_t n_sample, uint32_t* hist, cudaStream_t stream);
 
 int launch_gather_raw(const uint32_t* rows, uint64_t n_rows, uint32_t W, const int64_t* ids,
                       uint64_t n_ids, uint32_t* out, bool vec, int device, cudaStream_t stream);

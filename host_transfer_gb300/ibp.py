@@ -56,7 +56,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("W", ctypes.c_uint32), ("segments", ctypes.c_uint32), ("uniform", ctypes.c_uint32),
                 ("max_runs", ctypes.c_uint32), ("min_kept_bits", ctypes.c_uint32),
                 ("max_kept_bits", ctypes.c_uint32), ("metadata_bytes", ctypes.c_uint64),
-                ("device", ctypes.c_int)]
+                ("device", ctypes.c_int), ("prefix_words", ctypes.c_uint32)]
 
 
 def load():
@@ -79,6 +79,8 @@ def load():
         "ibp_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], i32),
         "ibp_plan_get_mask": ([vp, vp, vp], i32),
         "ibp_plan_set_hints": ([vp, u32], i32),
+        "ibp_plan_tune_prefix": ([vp, vp, u64, vp, u64, ctypes.POINTER(u32), vp], i32),
+        "ibp_plan_set_prefix": ([vp, u32], i32),
         "ibp_compress": ([vp, vp, vp, u64, vp, vp, vp], i32),
         "ibp_gather_decompress": ([vp, vp, u64, vp, vp, u64, vp, vp], i32),
         "ibp_decompress_contig": ([vp, vp, u64, vp, u64, u64, vp, vp], i32),
@@ -210,6 +212,10 @@ class Plan:
         """IBP_HINT_* access hints for later decompress calls (0 = default)."""
         _check(load().ibp_plan_set_hints(self.handle, int(hints)), "ibp_plan_set_hints")
 
+    def set_prefix(self, words: int):
+        """Words fetched from every slot before its headers are read (0 = default)."""
+        _check(load().ibp_plan_set_prefix(self.handle, int(words)), "ibp_plan_set_prefix")
+
     def mask_bitval(self):
         lib = load()
         m = torch.empty(self.W, dtype=torch.int32)
@@ -323,6 +329,20 @@ def ibp_row_lengths(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_
         _check(lib.ibp_row_lengths(plan.handle, _ptr(s), n, _ptr(bitmask), _ptr(row_ids), k,
                                    _ptr(out), _stream(stream, dev)), "ibp_row_lengths")
     return out
+
+
+def ibp_plan_tune_prefix(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, max_sample: int = 0,
+                         stream=None) -> int:
+    """Set the plan's prefix from the stored lengths of sampled rows of a
+    compressed table; returns the prefix in words.  Synchronises the stream."""
+    lib = load()
+    sp, n, W = _word_rows(slots)
+    got = ctypes.c_uint32(0)
+    dev = torch.device("cuda", plan.device)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_plan_tune_prefix(plan.handle, sp, n, _ptr(bitmask), int(max_sample), ctypes.byref(got),
+                                        _stream(stream, dev)), "ibp_plan_tune_prefix")
+    return int(got.value)
 
 
 def ibp_packed_offsets(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor,

@@ -88,6 +88,8 @@ typedef struct ibp_plan_info {
   uint32_t max_kept_bits;  /* most kept bits of any word position */
   uint64_t metadata_bytes; /* device bytes of the plan's tables (Mask + Bitval + derived) */
   int device;              /* CUDA device of the plan */
+  uint32_t prefix_words;   /* words a decompress call fetches from every slot before
+                              reading the row's headers (slot layout, aligned buffers) */
 } ibp_plan_info;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -188,6 +190,41 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out);
  * calls in flight.  Errors: IBP_EINVAL (NULL plan, unknown bits).
  */
 int ibp_plan_set_hints(ibp_plan* plan, uint32_t hints);
+
+/*
+ * Prefix length.  A decompress call first fetches the leading words of every
+ * requested slot, reads the row's participation headers there (« Algorithme
+ * central », step 3: the headers say how long the row's stream is), and then
+ * fetches whatever of the stream is left.  By default the prefix is the
+ * shortest stream the plan allows (Mask popcounts over every word position),
+ * so nothing is ever over-read; when the table's rows are longer than that -
+ * a Mask with few invariant bits in some positions, rows of mixed length - most
+ * rows need the second, dependent fetch, which over the host link costs a
+ * round trip and a partly re-read sector.
+ *
+ * ibp_plan_tune_prefix reads the headers of min(n_rows, max_sample) evenly
+ * spaced rows of a compressed table (row i * n_rows / n_sample; max_sample 0 =
+ * 65536), takes their stored lengths in 16-byte chunks (W for raw rows) and
+ * sets the prefix P (in chunks, from the default up to W) that minimises
+ * sum over sampled rows of (c > P ? c + 8 : P), c the row's chunks: words
+ * fetched plus a penalty of 8 chunks for each second fetch.  The prefix in
+ * words is written to *prefix_words when that is not NULL.  slots and bitmask
+ * are as for ibp_gather_decompress (host-mapped or device memory).
+ * Synchronises `stream`.  Errors: IBP_EINVAL, IBP_ENOMEM, IBP_ECUDA.
+ *
+ * ibp_plan_set_prefix sets it directly in words (0 restores the default; a
+ * value below the default counts as the default; capped at W).
+ *
+ * Both change speed, never results, and take effect for calls issued after
+ * they return.  They apply to the slot layout; the packed layout always uses
+ * the default, since a packed row may end before a longer prefix.  Neither
+ * has a counterpart in the paper: its decoder (« Algorithme central », step 3)
+ * has a warp read a row's contiguous compressed segment, without saying how
+ * the warp learns the segment's length before reading it.
+ */
+int ibp_plan_tune_prefix(ibp_plan* plan, const uint32_t* slots, uint64_t n_rows, const uint32_t* bitmask,
+                         uint64_t max_sample, uint32_t* prefix_words, void* stream);
+int ibp_plan_set_prefix(ibp_plan* plan, uint32_t words);
 
 /* The plan's Mask and Bitval (W words each) copied to host memory `mask` and
  * `bitval` (either may be NULL).  Synchronous. */

@@ -244,7 +244,8 @@ def test_out_of_range_ids_give_zero_rows_and_erange():
 
 
 @pytest.mark.parametrize("W", [40, 128])
-def test_corrupt_slots_give_zero_rows_and_ecorrupt(W):
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_corrupt_slots_give_zero_rows_and_ecorrupt(W, where):
     rng = np.random.default_rng(9)
     rows = _float_rows(rng, 64, W)
     g = gpu_codec(rows, rows, 0.9, "host")
@@ -254,7 +255,7 @@ def test_corrupt_slots_give_zero_rows_and_ecorrupt(W):
     slots[0, :S] = 0  # every word announces 32 bits: stream >= W words
     if W % 32:
         slots[1, S - 1] |= 1 << 31  # header bit past the last word
-    bad = pinned(slots)
+    bad = place(slots, where)
     ids = np.arange(4, dtype=np.int64)
     out = ibp.ibp_gather_decompress(g["plan"], bad, on_device(g["bitmask"]), torch.from_numpy(ids).cuda())
     code = ibp.ibp_get_status(g["plan"], raise_on_error=False)
@@ -420,3 +421,23 @@ def test_row_reuse_hint_same_results(where):
     assert np.array_equal(words_np(hinted), rows[ids])
     with pytest.raises(ibp.IbpError):
         g["plan"].set_hints(2)
+
+
+@pytest.mark.parametrize("W", [32, 512])
+def test_hbm_long_batches(W):
+    """Batches from HBM long enough that every decoding warp cycles through
+    its shared-memory stages many times, with a ragged last group."""
+    rng = np.random.default_rng(7 * W)
+    n = (3 << 21) // W + 13
+    rows = _float_rows(rng, n, W)
+    rows[::7] = rng.integers(0, 2**32, (len(rows[::7]), W), dtype=np.uint64).astype(np.uint32)
+    g, _ = _check_codec(rows, rows[:4096], 0.9, "hbm")
+    bm_t = on_device(g["bitmask"])
+    ids = rng.integers(0, n, 4 * n + 5).astype(np.int64)
+    out = ibp.ibp_gather_decompress(g["plan"], g["slots_t"], bm_t, torch.from_numpy(ids).cuda())
+    torch.cuda.synchronize()
+    assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
+    assert np.array_equal(words_np(out), rows[ids])
+    out = ibp.ibp_decompress_contig(g["plan"], g["slots_t"], bm_t, 3, n - 4)
+    torch.cuda.synchronize()
+    assert np.array_equal(words_np(out), rows[3:n - 1])
