@@ -30,13 +30,14 @@ int check_launch(const char* where) {
   return IBP_OK;
 }
 
-int resolve_ptr(const void* p, int device, const void** dev) {
+int resolve_ptr(const void* p, int device, const void** dev, int* on_device) {
   cudaPointerAttributes attr;
   cudaError_t e = cudaPointerGetAttributes(&attr, p);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return IBP_EINVAL;
   }
+  *on_device = 1;
   switch (attr.type) {
     case cudaMemoryTypeDevice:
       if (attr.device != device) return IBP_EINVAL;
@@ -48,10 +49,16 @@ int resolve_ptr(const void* p, int device, const void** dev) {
     case cudaMemoryTypeHost:
       if (attr.devicePointer == nullptr) return IBP_EINVAL;
       *dev = attr.devicePointer;
+      *on_device = 0;
       return IBP_OK;
     default:
       return IBP_EINVAL;  // pageable host memory
   }
+}
+
+int resolve_ptr(const void* p, int device, const void** dev) {
+  int on_device;
+  return resolve_ptr(p, device, dev, &on_device);
 }
 
 int sm_count(int device) {
@@ -361,7 +368,8 @@ static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64
   DeviceGuard g(plan->device);
   if (!g.ok) return IBP_ECUDA;
   const void *dsl, *dbm, *dout, *dids = nullptr;
-  if (resolve_ptr(slots, plan->device, &dsl) || resolve_ptr(bitmask, plan->device, &dbm) ||
+  int slots_on_device = 1;
+  if (resolve_ptr(slots, plan->device, &dsl, &slots_on_device) || resolve_ptr(bitmask, plan->device, &dbm) ||
       resolve_ptr(out, plan->device, &dout))
     return IBP_EINVAL;
   if (ids && resolve_ptr(ids, plan->device, &dids)) return IBP_EINVAL;
@@ -369,6 +377,7 @@ static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64
   if (offsets && resolve_ptr(offsets, plan->device, &doff)) return IBP_EINVAL;
   DecodeArgs a;
   a.offsets = static_cast<const uint64_t*>(doff);
+  a.dev_slots = static_cast<uint32_t>(slots_on_device);
   a.pv = plan->view;
   a.slots = static_cast<const uint32_t*>(dsl);
   a.bitmask = static_cast<const uint32_t*>(dbm);

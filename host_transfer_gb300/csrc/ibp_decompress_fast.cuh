@@ -31,9 +31,14 @@
 namespace ibp {
 
 constexpr int kFastWarps = 8;
-constexpr int kFastStages = 3;               // shared-memory stages per warp (D >= 3)
-constexpr uint32_t kFastGroupWords = 1024;   // rows per group G = this / W (at least 1)
+constexpr int kFastStages = 3;  // shared-memory stages per warp (D >= 3)
 constexpr uint32_t kAll = 0xFFFFFFFFu;
+// Words per group (GW; rows per group G = GW / W, at least 1).  512 by
+// default; 256 for copies that also allocate in L1 (IBP_HINT_ROW_REUSE on
+// host-mapped slots): the smaller stages leave more of the SM's on-chip
+// memory to L1, which is where repeated rows are found.
+constexpr uint32_t kGroupWords = 512;
+constexpr uint32_t kGroupWordsReuse = 256;
 
 // Words of a per-word table entry in shared memory: {run masks, packed run
 // shifts, Bitval & Mask}: 4 words for up to two runs, 8 for up to four.
@@ -50,10 +55,10 @@ struct TabShape {
   static constexpr uint32_t WORDS = ENT + EPL;  // shared words before the warp stages
 };
 
-template <int SC>
+template <int SC, uint32_t GW>
 struct FastShape {
   static constexpr uint32_t W = 32u * SC;
-  static constexpr uint32_t G = kFastGroupWords / W >= 1 ? kFastGroupWords / W : 1u;  // rows per group
+  static constexpr uint32_t G = GW / W >= 1 ? GW / W : 1u;  // rows per group
   static constexpr uint32_t STAGE = G * W + 32u;           // words per stage
   static constexpr uint32_t CH = W / 4;                    // 16-byte chunks per row
   static constexpr uint32_t CB = (CH + 31) / 32;           // chunk blocks of 32 per row
@@ -63,9 +68,9 @@ struct FastShape {
 // layout, row r is slots[offsets[r] .. offsets[r + 1]) (its stored words
 // rounded up to 16 bytes), and a row whose stream would reach past that
 // extent is corrupt.
-template <int R, int SC, int NPL, bool TAB, bool PK>
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW>
 __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const DecodeArgs a) {
-  using F = FastShape<SC>;
+  using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
   constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
   constexpr uint32_t EW = TabEntry<R>::EW;
@@ -393,9 +398,9 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   cp_wait<0>();
 }
 
-template <int R, int SC, int NPL, bool TAB, bool PK>
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW>
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  using F = FastShape<SC>;
+  using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
   const size_t per_warp = 4ull * kFastStages * F::STAGE;
   const size_t fixed = 4ull * T::WORDS;
@@ -403,7 +408,7 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = fixed + warps * per_warp;
-  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK>;
+  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
   // for this launch shape.
   static int occ_cache[64] = {0};
@@ -429,47 +434,51 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   return check_launch("k_decompress_fast");
 }
 
-template <int R, int NPL, bool TAB, bool PK>
+template <int R, int NPL, bool TAB, bool PK, uint32_t GW>
 static int launch_fast_sc(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   switch (plan->S) {
-    case 1: return launch_fast_t<R, 1, NPL, TAB, PK>(plan, a, stream);
-    case 2: return launch_fast_t<R, 2, NPL, TAB, PK>(plan, a, stream);
-    case 4: return launch_fast_t<R, 4, NPL, TAB, PK>(plan, a, stream);
-    case 8: return launch_fast_t<R, 8, NPL, TAB, PK>(plan, a, stream);
-    case 16: return launch_fast_t<R, 16, NPL, TAB, PK>(plan, a, stream);
-    case 32: return launch_fast_t<R, 32, NPL, TAB, PK>(plan, a, stream);
-    default: return launch_fast_t<R, 64, NPL, TAB, PK>(plan, a, stream);
+    case 1: return launch_fast_t<R, 1, NPL, TAB, PK, GW>(plan, a, stream);
+    case 2: return launch_fast_t<R, 2, NPL, TAB, PK, GW>(plan, a, stream);
+    case 4: return launch_fast_t<R, 4, NPL, TAB, PK, GW>(plan, a, stream);
+    case 8: return launch_fast_t<R, 8, NPL, TAB, PK, GW>(plan, a, stream);
+    case 16: return launch_fast_t<R, 16, NPL, TAB, PK, GW>(plan, a, stream);
+    case 32: return launch_fast_t<R, 32, NPL, TAB, PK, GW>(plan, a, stream);
+    default: return launch_fast_t<R, 64, NPL, TAB, PK, GW>(plan, a, stream);
   }
 }
 
-template <bool PK>
+template <bool PK, uint32_t GW>
 static int launch_fast_uniform_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   switch (plan->max_runs) {
-    case 1: return launch_fast_sc<1, 0, false, PK>(plan, a, stream);
-    case 2: return launch_fast_sc<2, 0, false, PK>(plan, a, stream);
-    case 3: return launch_fast_sc<3, 0, false, PK>(plan, a, stream);
-    default: return launch_fast_sc<4, 0, false, PK>(plan, a, stream);
+    case 1: return launch_fast_sc<1, 0, false, PK, GW>(plan, a, stream);
+    case 2: return launch_fast_sc<2, 0, false, PK, GW>(plan, a, stream);
+    case 3: return launch_fast_sc<3, 0, false, PK, GW>(plan, a, stream);
+    default: return launch_fast_sc<4, 0, false, PK, GW>(plan, a, stream);
   }
 }
 
-template <int R, bool PK>
+template <int R, bool PK, uint32_t GW>
 static int launch_table_r(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   switch (plan->view.npl) {
-    case 0: return launch_fast_sc<R, 0, true, PK>(plan, a, stream);
-    case 1: return launch_fast_sc<R, 1, true, PK>(plan, a, stream);
-    default: return launch_fast_sc<R, 6, true, PK>(plan, a, stream);
+    case 0: return launch_fast_sc<R, 0, true, PK, GW>(plan, a, stream);
+    case 1: return launch_fast_sc<R, 1, true, PK, GW>(plan, a, stream);
+    default: return launch_fast_sc<R, 6, true, PK, GW>(plan, a, stream);
   }
 }
 
-template <bool PK>
+template <bool PK, uint32_t GW>
 static int launch_fast_table_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  return plan->max_runs <= 2 ? launch_table_r<2, PK>(plan, a, stream) : launch_table_r<4, PK>(plan, a, stream);
+  return plan->max_runs <= 2 ? launch_table_r<2, PK, GW>(plan, a, stream)
+                             : launch_table_r<4, PK, GW>(plan, a, stream);
 }
 
 // One translation unit each (compiled in parallel): slot layout uniform and
-// table plans, packed layout uniform and table plans.
+// table plans with kGroupWords and with kGroupWordsReuse, packed layout
+// uniform and table plans (kGroupWords).
 int launch_fast_uniform(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+int launch_fast_uniform_reuse(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_table(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+int launch_fast_table_reuse(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_uniform_packed(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_table_packed(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 

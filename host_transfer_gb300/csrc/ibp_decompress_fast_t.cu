@@ -7,7 +7,7 @@
 namespace ibp {
 
 int launch_fast_table(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  return launch_fast_table_t<false>(plan, a, stream);
+  return launch_fast_table_t<false, kGroupWords>(plan, a, stream);
 }
 
 }  // namespace ibp

@@ -6,7 +6,7 @@
 namespace ibp {
 
 int launch_fast_table_packed(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  return launch_fast_table_t<true>(plan, a, stream);
+  return launch_fast_table_t<true, kGroupWords>(plan, a, stream);
 }
 
 }  // namespace ibp

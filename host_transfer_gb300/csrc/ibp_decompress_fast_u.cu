@@ -6,7 +6,7 @@
 namespace ibp {
 
 int launch_fast_uniform(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  return launch_fast_uniform_t<false>(plan, a, stream);
+  return launch_fast_uniform_t<false, kGroupWords>(plan, a, stream);
 }
 
 bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a) {
@@ -23,6 +23,8 @@ int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t str
   if (a.offsets)
     return plan->uniform ? launch_fast_uniform_packed(plan, a, stream)
                          : launch_fast_table_packed(plan, a, stream);
+  if ((a.pv.hints & IBP_HINT_ROW_REUSE) && !a.dev_slots)
+    return plan->uniform ? launch_fast_uniform_reuse(plan, a, stream) : launch_fast_table_reuse(plan, a, stream);
   return plan->uniform ? launch_fast_uniform(plan, a, stream) : launch_fast_table(plan, a, stream);
 }
 

@@ -5,7 +5,7 @@
 namespace ibp {
 
 int launch_fast_uniform_packed(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  return launch_fast_uniform_t<true>(plan, a, stream);
+  return launch_fast_uniform_t<true, kGroupWords>(plan, a, stream);
 }
 
 }  // namespace ibp

@@ -87,6 +87,9 @@ int check_launch(const char* where);
 // Accepts device memory of `device`, managed memory, and mapped pinned host
 // memory.  Returns IBP_OK or IBP_EINVAL.
 int resolve_ptr(const void* p, int device, const void** dev);
+// As resolve_ptr; also sets *on_device to 1 for device or managed memory and
+// to 0 for mapped host memory.
+int resolve_ptr(const void* p, int device, const void** dev, int* on_device);
 int sm_count(int device);
 
 // ---------------------------------------------------------------------------
@@ -106,6 +109,7 @@ struct DecodeArgs {
   uint32_t rowcap;         // stage words per row: W rounded up to a multiple of 32
   uint32_t pre;            // words fetched for every row before its headers are read
   uint32_t vec;            // 16-byte copies allowed
+  uint32_t dev_slots;      // slots in device (or managed) memory, not host-mapped
 };
 
 int launch_decompress(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);

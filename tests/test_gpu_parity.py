@@ -342,9 +342,10 @@ def test_row_lengths_match_oracle_stored_words(W):
     assert got[200] == 0 and got[201] == 0 and got[202] == want[7]
 
 
-def _explicit_plan_check(mask, bitval, rows, where="hbm"):
+def _explicit_plan_check(mask, bitval, rows, where="hbm", hints=0):
     """Compress + gather with an explicit Mask/Bitval; compare with the oracle."""
     plan = ibp.ibp_plan_create(torch.from_numpy(mask.view(np.int32)), torch.from_numpy(bitval.view(np.int32)))
+    plan.set_hints(hints)
     rows_t = place(rows, where)
     slots_t = empty_like_in(rows_t, where)
     _, bitmask, stored = ibp.ibp_compress(plan, rows_t, slots_t)
@@ -421,6 +422,29 @@ def test_row_reuse_hint_same_results(where):
     assert np.array_equal(words_np(hinted), rows[ids])
     with pytest.raises(ibp.IbpError):
         g["plan"].set_hints(2)
+
+
+@pytest.mark.parametrize("W", [32, 64, 128, 256, 512, 2048])
+@pytest.mark.parametrize("kind", ["uniform", "two_popcounts", "up_to_4_runs"])
+def test_row_reuse_hint_from_host_memory(W, kind):
+    """Row-reuse copies from host-mapped slots take kernels with smaller
+    groups; uniform and per-word plans, every segment count."""
+    rng = np.random.default_rng(3 * W + len(kind))
+    if kind == "uniform":
+        keep = np.full(W, _run_mask(0, 9) | _run_mask(23, 3), np.uint64)
+    elif kind == "two_popcounts":
+        keep = np.array([_run_mask(0, 27) | (1 << 31) if w % 3 else _run_mask(26, 4) for w in range(W)], np.uint64)
+    else:
+        keep = np.array([_run_mask(0, 3) | _run_mask(6, 2) | _run_mask(12, 5) | _run_mask(24, 1 + w % 7)
+                         for w in range(W)], np.uint64)
+    mask = (~keep & 0xFFFFFFFF).astype(np.uint32)
+    bitval = rng.integers(0, 2**32, 1 if kind == "uniform" else W, dtype=np.uint64).astype(np.uint32)
+    bitval = np.broadcast_to(bitval, (W,)) & mask
+    n = max(40, min(900, 300_000 // W))
+    rows = _rows_for(mask, bitval, rng, n)
+    rows[::11] = rng.integers(0, 2**32, (len(rows[::11]), W), dtype=np.uint64).astype(np.uint32)
+    plan = _explicit_plan_check(mask, bitval, rows, "host", hints=ibp.IBP_HINT_ROW_REUSE)
+    assert plan.info["uniform"] == (kind == "uniform")
 
 
 @pytest.mark.parametrize("W", [32, 512])
