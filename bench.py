@@ -164,7 +164,8 @@ def measured_peaks() -> dict:
 
 
 KERNEL_SOURCES = ["ibp_decompress_fast.cuh", "ibp_decompress_fast_u.cu", "ibp_decompress_fast_t.cu",
-                  "ibp_decompress.cu", "ibp_internal.cuh"]
+                  "ibp_decompress_fast_up.cu", "ibp_decompress_fast_tp.cu", "ibp_decompress_fast_ur.cu",
+                  "ibp_decompress_fast_tr.cu", "ibp_decompress.cu", "ibp_internal.cuh", "ibp_api.cu"]
 
 
 def kernel_sources_sha() -> str:
@@ -175,19 +176,22 @@ def kernel_sources_sha() -> str:
     return h.hexdigest()
 
 
-def kernel_traffic(kind: str) -> float | None:
-    """DRAM bytes per launch from the committed ncu summary, when it was taken
-    on the current kernel sources (else None)."""
+def kernel_traffic(kind: str) -> dict:
+    """Measured traffic per launch of one bench leg from the committed ncu
+    summary, when it was taken on the current kernel sources (else {}):
+    dram = DRAM bytes read + written; link = bytes over the host link
+    (sysmem sectors x 32)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         rec = json.load(open(path))
         sha = kernel_sources_sha()
     except (OSError, ValueError):
-        return None
+        return {}
     ent = rec.get(kind)
     if not ent or ent.get("kernel_source_sha256") != sha:
-        return None
-    return ent.get("bytes_per_launch")
+        return {}
+    return {"dram": ent.get("dram_bytes_read", 0) + ent.get("dram_bytes_write", 0),
+            "link": ent.get("link_bytes")}
 
 
 def workload_desc(name: str, n_rows: int) -> str:
@@ -245,6 +249,21 @@ def cpu_oracle_decode(slots, bitmask, mask, bitval, batches, seconds, threads):
         rows_done += len(ids)
         k += 1
     return rows_done * 4 * W / t_used / 1e9, rows_done, t_used
+
+
+def cpu_oracle_compress(rows, mask, bitval, seconds, threads):
+    """Time the C oracle compressing `rows` (repeated for about `seconds`);
+    returns (GB/s of uncompressed input, rows compressed, seconds)."""
+    from oracle import oracle_c
+
+    oracle_c.set_threads(threads)
+    rows_done, t_used = 0, 0.0
+    while t_used < seconds:
+        t0 = time.perf_counter()
+        oracle_c.compress(rows, mask, bitval)
+        t_used += time.perf_counter() - t0
+        rows_done += rows.shape[0]
+    return rows_done * 4 * rows.shape[1] / t_used / 1e9, rows_done, t_used
 
 
 # ---------------------------------------------------------------------------
@@ -529,7 +548,9 @@ def run_ours(args):
     host_achieved = link_bytes_launch / (launch_ms * 1e-3) / 1e9
     hbm_alg_bytes = (link_words * 4 + K * B * (4 * W + 8) + K * B / 8) / K
     hbm_achieved = hbm_alg_bytes / (hbm_launch_ms * 1e-3) / 1e9
+    traffic_host = kernel_traffic("host_resident")
     traffic_hbm = kernel_traffic("hbm_resident")
+    traffic_pk = kernel_traffic("packed_hbm_cache")
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -542,11 +563,14 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "space_saving_pct": round(100 * saving, 3),
         "compressed_fraction_batch": round(f_batch, 5),
+        "unique_ids_per_batch": round(float(np.mean([np.unique(b).size for b in batches])), 1),
         "h2d_gbs": round(h2d_gbs, 2),
         "host_ceiling_gbs": round(h2d_gbs / f_batch, 2),
         "frac_of_host_ceiling": round((B * 4 * W / (launch_ms * 1e-3) / 1e9) / (h2d_gbs / f_batch), 4),
         "roofline": {"bound": "host_link", "achieved": round(host_achieved, 2), "peak": round(h2d_gbs, 2),
-                     "unit": "GB/s", "frac": round(host_achieved / h2d_gbs, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(host_achieved / h2d_gbs, 4),
+                     "traffic": traffic_host.get("link"), "dram_traffic": traffic_host.get("dram"),
+                     "traffic_source": "ncu: host-link bytes (sysmem sectors x 32) and DRAM bytes per launch",
                      "peak_source": "cudaMemcpyAsync pinned->HBM of the 1 GB table, median of 10, same run",
                      "kernel": "k_decompress (host-resident slots)",
                      "bytes_per_launch": round(link_bytes_launch)},
@@ -554,7 +578,7 @@ def run_ours(args):
             "value": round(B * 4 * W / (hbm_total_ms / K * 1e-3) / 1e9, 3), "unit": "GB/s",
             "ms_per_step": round(hbm_total_ms / K, 4),
             "roofline": {"bound": "hbm", "achieved": round(hbm_achieved, 2), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(hbm_achieved / hbm_peak, 4), "traffic": traffic_hbm,
+                         "frac": round(hbm_achieved / hbm_peak, 4), "traffic": traffic_hbm.get("dram"),
                          "peak_source": "MEASURED_PEAKS.json hbm_gbs" if peaks.get("hbm_gbs") else "fallback",
                          "kernel": "k_decompress (HBM-resident slots)",
                          "bytes_per_launch": round(hbm_alg_bytes)}},
@@ -563,7 +587,7 @@ def run_ours(args):
             "ms_per_step": round(pk_ms, 4),
             "capacity_saving_pct": round(100 * (1 - packed_words / float(n * W)), 3),
             "roofline": {"bound": "hbm", "achieved": round(pk_achieved, 2), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(pk_achieved / hbm_peak, 4), "traffic": None,
+                         "frac": round(pk_achieved / hbm_peak, 4), "traffic": traffic_pk.get("dram"),
                          "kernel": "k_decompress_fast (packed layout)", "bytes_per_launch": round(pk_alg_bytes)}},
         "uncompressed_gather": {
             "zero_copy_host_gbs": round(K * B * 4 * W / (raw_host_ms * 1e-3) / 1e9, 3),
@@ -590,9 +614,19 @@ def run_ours(args):
                                              mask.cpu().numpy().view(np.uint32),
                                              bitval.cpu().numpy().view(np.uint32),
                                              batches, args.cpu_seconds, threads)
+        m_np, b_np = mask.cpu().numpy().view(np.uint32), bitval.cpu().numpy().view(np.uint32)
+        gbs1, nrows1, secs1 = cpu_oracle_decode(rows_np, bitmask.cpu().numpy().view(np.uint32), m_np, b_np,
+                                                batches, args.cpu_seconds / 4, 1)
+        sub = workloads.make_table(name, n_rows=min(n, 65536))  # the table's first rows, uncompressed
+        cgbs, crows, csecs = cpu_oracle_compress(sub, m_np, b_np, args.cpu_seconds / 4, threads)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{nrows} ids of the timed batches decoded by the bit-by-bit C "
-                                          f"oracle in {secs:.1f} s (OpenMP over rows)"}
+                                          f"oracle in {secs:.1f} s (OpenMP over rows)",
+                                "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                                                  "sample": f"{nrows1} ids decoded in {secs1:.1f} s"},
+                                "compress": {"value": round(cgbs, 4), "unit": "GB/s (input)", "cores": threads,
+                                             "sample": f"the table's first {sub.shape[0]} rows compressed "
+                                                       f"{crows // sub.shape[0]} times in {csecs:.1f} s"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
