@@ -375,7 +375,7 @@ static int decompress_common(const ibp_plan* plan, const uint32_t* slots, uint64
   if (ids && resolve_ptr(ids, plan->device, &dids)) return IBP_EINVAL;
   const void* doff = nullptr;
   if (offsets && resolve_ptr(offsets, plan->device, &doff)) return IBP_EINVAL;
-  DecodeArgs a;
+  DecodeArgs a{};
   a.offsets = static_cast<const uint64_t*>(doff);
   a.dev_slots = static_cast<uint32_t>(slots_on_device);
   a.pv = plan->view;
@@ -539,3 +539,125 @@ int ibp_gather_raw(const uint32_t* rows, uint64_t n_rows, uint32_t W, const int6
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Plan sets: one plan per block of consecutive rows (finer Mask granularity)
+
+struct ibp_plan_set {
+  int device;
+  uint32_t W, S, n, max_runs, npl;
+  std::vector<const ibp_plan*> plans;
+  ibp::PlanView* d_views;  // n views in device memory
+};
+
+int ibp_plan_set_create(const ibp_plan* const* plans, uint32_t n_plans, ibp_plan_set** out) {
+  g_detail[0] = 0;
+  if (!out) return IBP_EINVAL;
+  *out = nullptr;
+  if (!plans || n_plans == 0 || n_plans > 65535u || !plans[0]) return IBP_EINVAL;
+  const ibp_plan* p0 = plans[0];
+  const uint32_t S = p0->S, W = p0->W;
+  const bool pow2 = S == 1 || S == 2 || S == 4 || S == 8 || S == 16 || S == 32;
+  if (W != 32u * S || !pow2) return IBP_EINVAL;
+  std::vector<PlanView> views(n_plans);
+  uint32_t max_runs = 0, npl = 0;
+  for (uint32_t i = 0; i < n_plans; ++i) {
+    const ibp_plan* p = plans[i];
+    if (!p || p->device != p0->device || p->W != W || p->max_runs > static_cast<uint32_t>(kMaxRuns))
+      return IBP_EINVAL;
+    max_runs = p->max_runs > max_runs ? p->max_runs : max_runs;
+    npl = p->view.npl > npl ? p->view.npl : npl;
+    views[i] = p->view;
+  }
+  DeviceGuard g(p0->device);
+  if (!g.ok) return IBP_ECUDA;
+  ibp_plan_set* set = new (std::nothrow) ibp_plan_set();
+  if (!set) return IBP_ENOMEM;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&set->d_views), sizeof(PlanView) * n_plans);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete set;
+    return IBP_ENOMEM;
+  }
+  e = cudaMemcpy(set->d_views, views.data(), sizeof(PlanView) * n_plans, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "ibp_plan_set_create");
+    cudaGetLastError();
+    cudaFree(set->d_views);
+    delete set;
+    return IBP_ECUDA;
+  }
+  set->device = p0->device;
+  set->W = W;
+  set->S = S;
+  set->n = n_plans;
+  set->max_runs = max_runs;
+  set->npl = npl;
+  set->plans.assign(plans, plans + n_plans);
+  *out = set;
+  return IBP_OK;
+}
+
+int ibp_plan_set_destroy(ibp_plan_set* set) {
+  if (!set) return IBP_OK;
+  DeviceGuard g(set->device);
+  cudaError_t e = cudaFree(set->d_views);
+  delete set;
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "cudaFree");
+    return IBP_ECUDA;
+  }
+  return IBP_OK;
+}
+
+int ibp_decompress_contig_set(const ibp_plan_set* set, const uint32_t* slots, uint64_t rows_per_plan,
+                              const uint32_t* bitmask, uint32_t* out, void* stream) {
+  g_detail[0] = 0;
+  if (!set) return IBP_EINVAL;
+  if (rows_per_plan == 0) return IBP_OK;
+  if (!slots || !bitmask || !out) return IBP_EINVAL;
+  if (rows_per_plan >= (1ull << 31) / set->n) return IBP_EINVAL;  // every row id fits in 31 bits
+  const uint64_t n_rows = rows_per_plan * set->n;
+  DeviceGuard g(set->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void *dsl, *dbm, *dout;
+  int slots_on_device = 1;
+  if (resolve_ptr(slots, set->device, &dsl, &slots_on_device) || resolve_ptr(bitmask, set->device, &dbm) ||
+      resolve_ptr(out, set->device, &dout))
+    return IBP_EINVAL;
+  DecodeArgs a{};
+  a.pv = set->plans[0]->view;
+  a.slots = static_cast<const uint32_t*>(dsl);
+  a.bitmask = static_cast<const uint32_t*>(dbm);
+  a.n_rows = n_rows;
+  a.n_out = n_rows;
+  a.out = const_cast<uint32_t*>(static_cast<const uint32_t*>(dout));
+  a.vec = aligned16(a.slots) && aligned16(a.out);
+  if (!a.vec) return IBP_EINVAL;  // the set decoder is the 16-byte vector path
+  a.dev_slots = static_cast<uint32_t>(slots_on_device);
+  a.rowcap = set->W;
+  // the shortest of the plans' prefixes (each holds its row's S headers)
+  uint32_t pre = set->W;
+  for (const ibp_plan* p : set->plans) {
+    const uint32_t q = prefix_words(p, true);
+    pre = q < pre ? q : pre;
+  }
+  a.pre = pre;
+  a.G = 1;
+  a.plans = set->d_views;
+  a.rows_per_plan = rows_per_plan;
+  a.n_plans = set->n;
+  return launch_fast_set(set->plans[0], set->max_runs, set->npl, a, static_cast<cudaStream_t>(stream));
+}
+
+int ibp_plan_set_get_status(const ibp_plan_set* set, void* stream) {
+  g_detail[0] = 0;
+  if (!set) return IBP_EINVAL;
+  int first = IBP_OK;
+  for (const ibp_plan* p : set->plans) {
+    const int st = ibp_get_status(p, stream);
+    if (st == IBP_ECUDA) return st;
+    if (first == IBP_OK) first = st;
+  }
+  return first;
+}

@@ -68,8 +68,12 @@ struct FastShape {
 // layout, row r is slots[offsets[r] .. offsets[r + 1]) (its stored words
 // rounded up to 16 bytes), and a row whose stream would reach past that
 // extent is corrupt.
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW>
+// MP = true (plan sets, contiguous decode, table path): CTA row blockIdx.y
+// decodes rows [y * rows_per_plan, (y + 1) * rows_per_plan) of the table with
+// plan y of a.plans (a device array of plan views).
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false>
 __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const DecodeArgs a) {
+  static_assert(!MP || (TAB && !PK), "plan sets decode through the table path, slot layout");
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
   constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
@@ -85,15 +89,25 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   const uint32_t lt = lanemask_lt();
   const uint32_t lanebit = 1u << lane;
 
+  // this CTA's plan, row range and output
+  PlanView pv;
+  if constexpr (MP)
+    pv = a.plans[blockIdx.y];
+  else
+    pv = a.pv;
+  const uint64_t n_out = MP ? a.rows_per_plan : a.n_out;
+  const uint64_t first = MP ? a.first + blockIdx.y * a.rows_per_plan : a.first;
+  uint32_t* const out = MP ? a.out + blockIdx.y * a.rows_per_plan * (32ull * SC) : a.out;
+
   // plan constants: uniform Mask (TAB = false) or the per-word tables
-  const uint32_t p = TAB ? a.pv.p_min : a.pv.u_p;
-  const uint32_t pscale = a.pv.p_scale;
-  const uint32_t bm = a.pv.u_bm;
+  const uint32_t p = TAB ? pv.p_min : pv.u_p;
+  const uint32_t pscale = pv.p_scale;
+  const uint32_t bm = pv.u_bm;
   uint32_t rm[R], rs[R];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
-    rm[k] = a.pv.u_rmask[k];
-    rs[k] = a.pv.u_rsh[k];
+    rm[k] = pv.u_rmask[k];
+    rs[k] = pv.u_rsh[k];
   }
   if constexpr (TAB) {
     // Stage the tables once per CTA; every thread reaches this barrier
@@ -101,24 +115,24 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
     for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
       uint32_t* e = tab + w * EW;
 #pragma unroll
-      for (int k = 0; k < (EW == 4 ? 2 : 4); ++k) e[k] = k < R ? __ldg(a.pv.rmask + k * W + w) : 0u;
-      e[EW == 4 ? 2 : 4] = __ldg(a.pv.rshift + w);
-      e[EW == 4 ? 3 : 5] = __ldg(a.pv.bm + w);
+      for (int k = 0; k < (EW == 4 ? 2 : 4); ++k) e[k] = k < R ? __ldg(pv.rmask + k * W + w) : 0u;
+      e[EW == 4 ? 2 : 4] = __ldg(pv.rshift + w);
+      e[EW == 4 ? 3 : 5] = __ldg(pv.bm + w);
     }
     if constexpr (NPL > 0) {
       for (uint32_t i = threadIdx.x; i < SC * NPL; i += blockDim.x)
-        epl[i] = __ldg(a.pv.eplanes + (i / NPL) * kPlanes + (i % NPL));
+        epl[i] = __ldg(pv.eplanes + (i / NPL) * kPlanes + (i % NPL));
     }
     __syncthreads();
   }
-  const bool reuse = (a.pv.hints & IBP_HINT_ROW_REUSE) != 0;
+  const bool reuse = (pv.hints & IBP_HINT_ROW_REUSE) != 0;
   const uint32_t pre = a.pre;          // multiple of 4, <= W
   const uint32_t pre_ch = pre >> 2;    // prefix chunks per row
   const uint32_t n_rows32 = static_cast<uint32_t>(a.n_rows);  // < 2^31 (checked by the launcher)
 
   // Warp gw owns groups gw, gw + nwarps, ...; group g is output rows
   // g*G .. g*G + G - 1 and lane q < G owns row g*G + q.
-  const uint64_t n_groups = (a.n_out + G - 1) / G;
+  const uint64_t n_groups = (n_out + G - 1) / G;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw_cta + warp;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw_cta;
   if (gw >= n_groups) return;  // warp-uniform; only warp-level syncs below
@@ -130,8 +144,8 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   constexpr int32_t kNoRow = -1, kBadId = -2;
   auto load_id = [&](uint64_t j, uint64_t rbase) -> int32_t {
     const uint64_t i = rbase + lane;
-    if (j >= J || lane >= G || i >= a.n_out) return kNoRow;
-    const int64_t id = a.ids ? a.ids[i] : static_cast<int64_t>(a.first + i);
+    if (j >= J || lane >= G || i >= n_out) return kNoRow;
+    const int64_t id = a.ids ? a.ids[i] : static_cast<int64_t>(first + i);
     return (id >= 0 && static_cast<uint64_t>(id) < n_rows32) ? static_cast<int32_t>(id) : kBadId;
   };
 
@@ -303,7 +317,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   };
 
   auto decode_group = [&](const uint32_t* sb, uint64_t rbase, uint32_t kind) {
-    uint32_t* const obase = a.out + rbase * W + lane;
+    uint32_t* const obase = out + rbase * W + lane;
     const uint32_t comp = __ballot_sync(kAll, kind == kComp);
     const uint32_t raw = __ballot_sync(kAll, kind == kRaw);
     const bool bad = kind == kBadRange || kind == kCorrupt;
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
       if ((comp >> q) & 1u) decode_row(sb + q * W, obase + q * W);
     }
     if (raw | badm) {
-      if (bad) record_status(a.pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
+      if (bad) record_status(pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
       for (uint32_t q = 0; q < G; ++q) {
         const bool r = (raw >> q) & 1u, z = (badm >> q) & 1u;
         if (!(r | z)) continue;
@@ -398,7 +412,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
   cp_wait<0>();
 }
 
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW>
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false>
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -408,7 +422,7 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = fixed + warps * per_warp;
-  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW>;
+  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW, MP>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
   // for this launch shape.
   static int occ_cache[64] = {0};
@@ -426,10 +440,11 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
     }
     occ_cache[dev] = occ;
   }
-  const uint64_t groups = (a.n_out + F::G - 1) / F::G;
+  const uint64_t groups = ((MP ? a.rows_per_plan : a.n_out) + F::G - 1) / F::G;
   const uint64_t need = (groups + warps - 1) / warps;
-  const uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
-  const unsigned grid = static_cast<unsigned>(need < cap ? need : cap);
+  uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
+  if (MP) cap = cap / a.n_plans > 0 ? cap / a.n_plans : 1;  // CTAs per plan
+  const dim3 grid(static_cast<unsigned>(need < cap ? need : cap), MP ? a.n_plans : 1u);
   kern<<<grid, static_cast<unsigned>(warps * 32), smem, stream>>>(a);
   return check_launch("k_decompress_fast");
 }
@@ -470,6 +485,18 @@ template <bool PK, uint32_t GW>
 static int launch_fast_table_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   return plan->max_runs <= 2 ? launch_table_r<2, PK, GW>(plan, a, stream)
                              : launch_table_r<4, PK, GW>(plan, a, stream);
+}
+
+template <int R, int NPL>
+static int launch_fast_set_sc(const ibp_plan* plan0, DecodeArgs& a, cudaStream_t stream) {
+  switch (plan0->S) {
+    case 1: return launch_fast_t<R, 1, NPL, true, false, kGroupWords, true>(plan0, a, stream);
+    case 2: return launch_fast_t<R, 2, NPL, true, false, kGroupWords, true>(plan0, a, stream);
+    case 4: return launch_fast_t<R, 4, NPL, true, false, kGroupWords, true>(plan0, a, stream);
+    case 8: return launch_fast_t<R, 8, NPL, true, false, kGroupWords, true>(plan0, a, stream);
+    case 16: return launch_fast_t<R, 16, NPL, true, false, kGroupWords, true>(plan0, a, stream);
+    default: return launch_fast_t<R, 32, NPL, true, false, kGroupWords, true>(plan0, a, stream);
+  }
 }
 
 // One translation unit each (compiled in parallel): slot layout uniform and

@@ -110,6 +110,10 @@ struct DecodeArgs {
   uint32_t pre;            // words fetched for every row before its headers are read
   uint32_t vec;            // 16-byte copies allowed
   uint32_t dev_slots;      // slots in device (or managed) memory, not host-mapped
+  // plan sets: row block y of rows_per_plan rows is decoded with plans[y]
+  const PlanView* plans;   // device array of n_plans views, or nullptr
+  uint64_t rows_per_plan;
+  uint32_t n_plans;
 };
 
 int launch_decompress(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
@@ -118,6 +122,10 @@ int launch_decompress(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 // 2^31 rows (ibp_decompress_fast.cu).
 bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a);
 int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+// Plan sets (ibp_decompress_fast_set.cu): contiguous decode through the
+// specialised kernel's table path with the set's most runs (2 or 4) and
+// e-planes (0, 1 or 6); W = 32 * S, S <= 32, 16-byte aligned buffers.
+int launch_fast_set(const ibp_plan* plan0, uint32_t max_runs, uint32_t npl, DecodeArgs& a, cudaStream_t stream);
 
 // Packed cache layout (ibp_packed.cu): per-row stored lengths rounded up to
 // 4 words and their exclusive scan; the copy of slots into packed rows.

@@ -81,6 +81,10 @@ def load():
         "ibp_plan_set_hints": ([vp, u32], i32),
         "ibp_plan_tune_prefix": ([vp, vp, u64, vp, u64, ctypes.POINTER(u32), vp], i32),
         "ibp_plan_set_prefix": ([vp, u32], i32),
+        "ibp_plan_set_create": ([ctypes.POINTER(vp), u32, ctypes.POINTER(vp)], i32),
+        "ibp_plan_set_destroy": ([vp], i32),
+        "ibp_decompress_contig_set": ([vp, vp, u64, vp, vp, vp], i32),
+        "ibp_plan_set_get_status": ([vp, vp], i32),
         "ibp_compress": ([vp, vp, vp, u64, vp, vp, vp], i32),
         "ibp_gather_decompress": ([vp, vp, u64, vp, vp, u64, vp, vp], i32),
         "ibp_decompress_contig": ([vp, vp, u64, vp, u64, u64, vp, vp], i32),
@@ -329,6 +333,58 @@ def ibp_row_lengths(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_
         _check(lib.ibp_row_lengths(plan.handle, _ptr(s), n, _ptr(bitmask), _ptr(row_ids), k,
                                    _ptr(out), _stream(stream, dev)), "ibp_row_lengths")
     return out
+
+
+class PlanSet:
+    """Plans for consecutive row blocks of one table (finer Mask granularity).
+    Keeps its plans alive; frees itself."""
+
+    def __init__(self, plans):
+        lib = load()
+        self.plans = list(plans)
+        if not self.plans:
+            raise ValueError("a plan set needs at least one plan")
+        arr = (ctypes.c_void_p * len(self.plans))(*[p.handle.value for p in self.plans])
+        h = ctypes.c_void_p()
+        _check(lib.ibp_plan_set_create(arr, len(self.plans), ctypes.byref(h)), "ibp_plan_set_create")
+        self.handle = h
+        self.W = self.plans[0].W
+        self.device = self.plans[0].device
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.ibp_plan_set_destroy(self.handle)
+            self.handle = None
+
+
+def ibp_plan_set_create(plans) -> PlanSet:
+    return PlanSet(plans)
+
+
+def ibp_decompress_contig_set(pset: PlanSet, slots: torch.Tensor, rows_per_plan: int, bitmask: torch.Tensor,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode n_plans * rows_per_plan rows; row block k with plan k."""
+    lib = load()
+    sp, n, W = _word_rows(slots)
+    dev = torch.device("cuda", pset.device)
+    total = rows_per_plan * len(pset.plans)
+    if n < total:
+        raise ValueError(f"slots hold {n} rows, the set decodes {total}")
+    if out is None:
+        out = torch.empty((total, W), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.ibp_decompress_contig_set(pset.handle, sp, int(rows_per_plan), _ptr(bitmask), _ptr(out),
+                                             _stream(stream, dev)), "ibp_decompress_contig_set")
+    return out
+
+
+def ibp_plan_set_get_status(pset: PlanSet, stream=None, raise_on_error: bool = True) -> int:
+    lib = load()
+    dev = torch.device("cuda", pset.device)
+    code = lib.ibp_plan_set_get_status(pset.handle, _stream(stream, dev))
+    if raise_on_error and code != IBP_OK:
+        raise IbpError(code, "ibp_plan_set_get_status")
+    return code
 
 
 def ibp_plan_tune_prefix(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, max_sample: int = 0,

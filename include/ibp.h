@@ -78,6 +78,7 @@ typedef enum ibp_status {
 
 /* Opaque per-device plan: Mask, Bitval and the derived decode tables. */
 typedef struct ibp_plan ibp_plan;
+typedef struct ibp_plan_set ibp_plan_set;
 
 typedef struct ibp_plan_info {
   uint32_t W;              /* words per row */
@@ -321,6 +322,42 @@ int ibp_gather_decompress_packed(const ibp_plan* plan, const uint32_t* packed,
                                  const uint64_t* offsets, uint64_t n_rows,
                                  const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
                                  uint32_t* out, void* stream);
+
+/*
+ * Plan sets - finer Mask granularity.  « Résultats » reports its savings per
+ * tensor (one Mask/Bitval per tensor); an attention KV cache mixes heads whose
+ * values have different scales, so one Mask for the whole tensor finds almost
+ * no invariant bits.  A plan set gives each block of consecutive rows its own
+ * plan (for a KV cache laid out [head][position][dim]: one plan per head) and
+ * decodes all the blocks in one launch.
+ *
+ * ibp_plan_set_create: plans[0 .. n_plans) (1 <= n_plans <= 65535), all on
+ * one device with the same W, W = 32 * S with S in {1, 2, 4, 8, 16, 32}, each
+ * with at most 4 runs of kept bits per word.  The set copies the plans' device
+ * views (table addresses, status word, hints) once: the plans must outlive
+ * the set, and hints set later are not seen by it.  Synchronous.  Errors:
+ * IBP_EINVAL, IBP_ENOMEM, IBP_ECUDA.  ibp_plan_set_destroy frees it (NULL is
+ * ignored).
+ *
+ * ibp_decompress_contig_set: the table is n_plans * rows_per_plan slots of W
+ * words; row k * rows_per_plan + i was compressed with plans[k] and is decoded
+ * with it into out row k * rows_per_plan + i.  bitmask covers all the rows
+ * (bit r of word r / 32): when rows_per_plan is a multiple of 32, compressing
+ * block k with plans[k] into bitmask + k * rows_per_plan / 32 builds it.
+ * slots (host-mapped or device memory) and out (n_plans * rows_per_plan * W
+ * words, device-accessible) must be 16-byte aligned; n_plans * rows_per_plan
+ * < 2^31.  Each row is fetched with the shortest prefix of the set's plans.
+ * Data errors are recorded in the status word of the row's plan.
+ * Asynchronous on `stream`.  Errors: IBP_EINVAL, IBP_ECUDA.
+ *
+ * ibp_plan_set_get_status: ibp_get_status of every plan of the set (each is
+ * cleared); returns the first error found (IBP_OK if none).
+ */
+int ibp_plan_set_create(const ibp_plan* const* plans, uint32_t n_plans, ibp_plan_set** out);
+int ibp_plan_set_destroy(ibp_plan_set* set);
+int ibp_decompress_contig_set(const ibp_plan_set* set, const uint32_t* slots, uint64_t rows_per_plan,
+                              const uint32_t* bitmask, uint32_t* out, void* stream);
+int ibp_plan_set_get_status(const ibp_plan_set* set, void* stream);
 
 /*
  * Synchronises `stream`, returns the first data error recorded by the plan's
