@@ -568,6 +568,7 @@ int ibp_plan_set_create(const ibp_plan* const* plans, uint32_t n_plans, ibp_plan
     max_runs = p->max_runs > max_runs ? p->max_runs : max_runs;
     npl = p->view.npl > npl ? p->view.npl : npl;
     views[i] = p->view;
+    views[i].pre = prefix_words(p, true);  // the plan's own prefix, as of now
   }
   DeviceGuard g(p0->device);
   if (!g.ok) return IBP_ECUDA;
@@ -636,13 +637,7 @@ int ibp_decompress_contig_set(const ibp_plan_set* set, const uint32_t* slots, ui
   if (!a.vec) return IBP_EINVAL;  // the set decoder is the 16-byte vector path
   a.dev_slots = static_cast<uint32_t>(slots_on_device);
   a.rowcap = set->W;
-  // the shortest of the plans' prefixes (each holds its row's S headers)
-  uint32_t pre = set->W;
-  for (const ibp_plan* p : set->plans) {
-    const uint32_t q = prefix_words(p, true);
-    pre = q < pre ? q : pre;
-  }
-  a.pre = pre;
+  a.pre = set->W;  // each CTA takes its plan's prefix from the device views
   a.G = 1;
   a.plans = set->d_views;
   a.rows_per_plan = rows_per_plan;

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_decompress_fast(const Decod
     __syncthreads();
   }
   const bool reuse = (pv.hints & IBP_HINT_ROW_REUSE) != 0;
-  const uint32_t pre = a.pre;          // multiple of 4, <= W
+  const uint32_t pre = MP ? pv.pre : a.pre;  // multiple of 4, <= W
   const uint32_t pre_ch = pre >> 2;    // prefix chunks per row
   const uint32_t n_rows32 = static_cast<uint32_t>(a.n_rows);  // < 2^31 (checked by the launcher)
 

@@ -55,6 +55,7 @@ struct PlanView {
   uint32_t* status;
   uint32_t p_min, p_scale, npl;
   uint32_t hints;  // IBP_HINT_* bits set by ibp_plan_set_hints
+  uint32_t pre;    // words fetched before the headers (read from device views of plan sets)
   // Uniform plans (every word position has the same Mask/Bitval): scalars.
   uint32_t u_mask, u_bm, u_p, u_keep;
   uint32_t u_rmask[kMaxRuns];

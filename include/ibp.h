@@ -335,7 +335,7 @@ int ibp_gather_decompress_packed(const ibp_plan* plan, const uint32_t* packed,
  * one device with the same W, W = 32 * S with S in {1, 2, 4, 8, 16, 32}, each
  * with at most 4 runs of kept bits per word.  The set copies the plans' device
  * views (table addresses, status word, hints) once: the plans must outlive
- * the set, and hints set later are not seen by it.  Synchronous.  Errors:
+ * the set, and hints or prefixes set later are not seen by it.  Synchronous.  Errors:
  * IBP_EINVAL, IBP_ENOMEM, IBP_ECUDA.  ibp_plan_set_destroy frees it (NULL is
  * ignored).
  *
@@ -346,7 +346,8 @@ int ibp_gather_decompress_packed(const ibp_plan* plan, const uint32_t* packed,
  * block k with plans[k] into bitmask + k * rows_per_plan / 32 builds it.
  * slots (host-mapped or device memory) and out (n_plans * rows_per_plan * W
  * words, device-accessible) must be 16-byte aligned; n_plans * rows_per_plan
- * < 2^31.  Each row is fetched with the shortest prefix of the set's plans.
+ * < 2^31.  Each row is fetched with its plan's prefix as it was when the set
+ * was created (tune the plans' prefixes first).
  * Data errors are recorded in the status word of the row's plan.
  * Asynchronous on `stream`.  Errors: IBP_EINVAL, IBP_ECUDA.
  *
