@@ -540,6 +540,43 @@ int ibp_gather_raw(const uint32_t* rows, uint64_t n_rows, uint32_t W, const int6
 
 }  // extern "C"
 
+int ibp_gather_decompress_bag(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                              const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
+                              const int64_t* bag_offsets, uint64_t n_bags, uint32_t mode, float* out,
+                              void* stream) {
+  g_detail[0] = 0;
+  if (!plan) return IBP_EINVAL;
+  if (n_bags == 0) return IBP_OK;
+  if (!slots || !bitmask || !bag_offsets || !out || n_rows == 0 || mode > IBP_BAG_MEAN) return IBP_EINVAL;
+  if ((n_ids > 0 && !row_ids) || n_rows >= (1ull << 31) || n_ids > (1ull << 40) || n_bags > (1ull << 40))
+    return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void *dsl, *dbm, *doff, *dout, *dids = nullptr;
+  if (resolve_ptr(slots, plan->device, &dsl) || resolve_ptr(bitmask, plan->device, &dbm) ||
+      resolve_ptr(bag_offsets, plan->device, &doff) || resolve_ptr(out, plan->device, &dout))
+    return IBP_EINVAL;
+  if (row_ids && resolve_ptr(row_ids, plan->device, &dids)) return IBP_EINVAL;
+  BagArgs a{};
+  DecodeArgs& d = a.d;
+  d.pv = plan->view;
+  d.slots = static_cast<const uint32_t*>(dsl);
+  d.bitmask = static_cast<const uint32_t*>(dbm);
+  d.ids = static_cast<const int64_t*>(dids);
+  d.n_rows = n_rows;
+  d.n_out = n_ids;
+  d.vec = (plan->W % 4 == 0) && aligned16(d.slots);
+  d.rowcap = ((plan->W + 31) / 32) * 32;
+  d.pre = prefix_words(plan, d.vec != 0);
+  d.G = 1;
+  a.offsets = static_cast<const int64_t*>(doff);
+  a.n_ids = n_ids;
+  a.n_bags = n_bags;
+  a.out = static_cast<float*>(const_cast<void*>(dout));
+  a.mean = mode;
+  return launch_bag(plan, a, static_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------------------------
 // Plan sets: one plan per block of consecutive rows (finer Mask granularity)
 

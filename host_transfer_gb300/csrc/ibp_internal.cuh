@@ -123,6 +123,18 @@ int launch_decompress(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 // 2^31 rows (ibp_decompress_fast.cu).
 bool fast_decompress_applies(const ibp_plan* plan, const DecodeArgs& a);
 int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+// Gather-decompress fused with sum / mean pooling (ibp_bag.cu).
+struct BagArgs {
+  DecodeArgs d;            // plan, slots, bitmask, ids, n_rows, pre, vec (n_out unused)
+  const int64_t* offsets;  // n_bags + 1 bag boundaries into ids
+  uint64_t n_ids;
+  uint64_t n_bags;
+  float* out;              // n_bags x W
+  uint32_t mean;           // 0: sum, 1: mean
+};
+// Specialised shapes only (as fast_decompress_applies, S <= 16); else IBP_EINVAL.
+int launch_bag(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
+
 // Plan sets (ibp_decompress_fast_set.cu): contiguous decode through the
 // specialised kernel's table path with the set's most runs (2 or 4) and
 // e-planes (0, 1 or 6); W = 32 * S, S <= 32, 16-byte aligned buffers.

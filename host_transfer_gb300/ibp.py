@@ -81,6 +81,7 @@ def load():
         "ibp_plan_set_hints": ([vp, u32], i32),
         "ibp_plan_tune_prefix": ([vp, vp, u64, vp, u64, ctypes.POINTER(u32), vp], i32),
         "ibp_plan_set_prefix": ([vp, u32], i32),
+        "ibp_gather_decompress_bag": ([vp, vp, u64, vp, vp, u64, vp, u64, u32, vp, vp], i32),
         "ibp_plan_set_create": ([ctypes.POINTER(vp), u32, ctypes.POINTER(vp)], i32),
         "ibp_plan_set_destroy": ([vp], i32),
         "ibp_decompress_contig_set": ([vp, vp, u64, vp, vp, vp], i32),
@@ -332,6 +333,37 @@ def ibp_row_lengths(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_
     with torch.cuda.device(dev):
         _check(lib.ibp_row_lengths(plan.handle, _ptr(s), n, _ptr(bitmask), _ptr(row_ids), k,
                                    _ptr(out), _stream(stream, dev)), "ibp_row_lengths")
+    return out
+
+
+IBP_BAG_SUM = 0
+IBP_BAG_MEAN = 1
+
+
+def ibp_gather_decompress_bag(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_ids: torch.Tensor,
+                              bag_offsets: torch.Tensor, mode: int = IBP_BAG_SUM,
+                              out: torch.Tensor | None = None, stream=None,
+                              n_rows: int | None = None) -> torch.Tensor:
+    """Pooled rows per bag (float32 device tensor [n_bags, W]) of the rows
+    row_ids[bag_offsets[b] .. bag_offsets[b+1])."""
+    lib = load()
+    sp, n, W = _word_rows(slots)
+    if W != plan.W:
+        raise ValueError(f"slots have {W} words, plan has {plan.W}")
+    for name, t in (("row_ids", row_ids), ("bag_offsets", bag_offsets)):
+        if t.dtype != torch.int64 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int64 tensor")
+    n_bags = bag_offsets.numel() - 1
+    dev = torch.device("cuda", plan.device)
+    if out is None:
+        out = torch.empty((max(n_bags, 0), W), dtype=torch.float32, device=dev)
+    if n_bags <= 0:
+        return out
+    with torch.cuda.device(dev):
+        _check(lib.ibp_gather_decompress_bag(plan.handle, sp, n if n_rows is None else n_rows, _ptr(bitmask),
+                                             _ptr(row_ids) if row_ids.numel() else None, row_ids.numel(),
+                                             _ptr(bag_offsets), n_bags, int(mode), _ptr(out),
+                                             _stream(stream, dev)), "ibp_gather_decompress_bag")
     return out
 
 

@@ -324,6 +324,40 @@ int ibp_gather_decompress_packed(const ibp_plan* plan, const uint32_t* packed,
                                  uint32_t* out, void* stream);
 
 /*
+ * Gather-decompress fused with pooling (an "embedding bag").  « Résultats »:
+ * IBP's rows feed DLRM embedding tables and GNN feature aggregation, whose
+ * consumer pools the rows of each bag; « Algorithme central », step 3: the
+ * fetch overlaps the logic that consumes the data.  Here the decoded rows are
+ * added in registers and never written out: only one pooled row per bag is.
+ *
+ * Rows are W float32 values (the decoded words read as IEEE single).  Bag b
+ * holds the id positions k in [bag_offsets[b], bag_offsets[b+1]).
+ * IBP_BAG_SUM: out[b] = row(row_ids[k0]) + row(row_ids[k0+1]) + ..., added in
+ * IEEE single precision in increasing k from +0.0 (no reassociation, no fused
+ * multiply-add): bit-identical to gather-decompress followed by that loop.
+ * IBP_BAG_MEAN: that sum divided by the bag size (one correctly rounded
+ * division); an empty bag gives zeros in both modes.
+ *
+ * slots, bitmask, n_rows  as for ibp_gather_decompress; W = 32 * 2^k <= 512,
+ *                 at most 4 runs of kept bits per word, slots 16-byte aligned,
+ *                 n_rows < 2^31 (IBP_EINVAL otherwise).
+ * row_ids     device-accessible int64[n_ids] (may be NULL when n_ids == 0).
+ * bag_offsets device-accessible int64[n_bags + 1].  A bag whose offsets are
+ *             not 0 <= bag_offsets[b] <= bag_offsets[b+1] <= n_ids gives zeros
+ *             and records IBP_ERANGE.
+ * out         device-accessible float[n_bags * W].
+ * Data errors as in ibp_gather_decompress: a bad id or a corrupt slot adds a
+ * zero row (it still counts in the bag's size) and records IBP_ERANGE /
+ * IBP_ECORRUPT.  Asynchronous on `stream`.  Errors: IBP_EINVAL, IBP_ECUDA.
+ */
+#define IBP_BAG_SUM 0u
+#define IBP_BAG_MEAN 1u
+int ibp_gather_decompress_bag(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
+                              const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
+                              const int64_t* bag_offsets, uint64_t n_bags, uint32_t mode, float* out,
+                              void* stream);
+
+/*
  * Plan sets - finer Mask granularity.  « Résultats » reports its savings per
  * tensor (one Mask/Bitval per tensor); an attention KV cache mixes heads whose
  * values have different scales, so one Mask for the whole tensor finds almost
