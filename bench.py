@@ -490,6 +490,39 @@ def run_ours(args):
     parity = parity and bool(np.array_equal(out.cpu().numpy().view(np.uint32), expect_last))
     del g_host, g_hbm
 
+    # ---- fused consumer: gather-decompress + sum pooling (embedding bag) ----
+    # Bags of POOLING consecutive ids of each batch; the fused call writes one
+    # pooled row per bag.  Unfused reference: gather-decompress, then torch's
+    # sum over each bag.
+    POOLING = 32
+    n_bags = B // POOLING
+    bag_off = torch.arange(0, n_bags * POOLING + 1, POOLING, dtype=torch.int64, device=dev)
+    bag_out = torch.empty((n_bags, W), dtype=torch.float32, device=dev)
+    bag_ref = torch.empty((n_bags, W), dtype=torch.float32, device=dev)
+    bag_res = {}
+    for where, src in (("host", table), ("hbm", table_d)):
+        fused_ms = time_steps(lambda k: ibp.ibp_gather_decompress_bag(plan, src, bitmask, ids_d[k], bag_off, out=bag_out),
+                              K, WU, f"bag_{where}_timed") / K
+        ibp.ibp_get_status(plan)
+        # the last timed batch's bags against its decoded rows added in order
+        ibp.ibp_gather_decompress(plan, src, bitmask, ids_d[last], out=out)
+        rows_f = out[:n_bags * POOLING].view(torch.float32).view(n_bags, POOLING, W)
+        bag_ref.zero_()
+        for j in range(POOLING):
+            bag_ref += rows_f[:, j]
+        bag_ok = bool(torch.equal(bag_out.view(torch.int32), bag_ref.view(torch.int32)))
+
+        def unfused(k):
+            ibp.ibp_gather_decompress(plan, src, bitmask, ids_d[k], out=out)
+            torch.sum(out[:n_bags * POOLING].view(torch.float32).view(n_bags, POOLING, W), dim=1, out=bag_ref)
+
+        unfused_ms = time_steps(unfused, K, WU, f"bag_unfused_{where}_timed") / K
+        bag_res[where] = {"value": round(n_bags * POOLING * 4 * W / (fused_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+                          "ms_per_step": round(fused_ms, 4), "unfused_ms_per_step": round(unfused_ms, 4),
+                          "speedup_vs_unfused": round(unfused_ms / fused_ms, 3),
+                          "parity": "bit-exact" if bag_ok else "MISMATCH"}
+        parity = parity and bag_ok
+
     # ---- packed HBM cache: only the stored words of each row ---------------
     offsets = ibp.ibp_packed_offsets(plan, table, bitmask)
     packed_words = int(offsets[-1].item())
@@ -589,6 +622,10 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": round(pk_achieved, 2), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(pk_achieved / hbm_peak, 4), "traffic": traffic_pk.get("dram"),
                          "kernel": "k_decompress_fast (packed layout)", "bytes_per_launch": round(pk_alg_bytes)}},
+        "bag_fused": {"what": f"gather-decompress fused with sum pooling, bags of {POOLING} ids "
+                              f"({n_bags} per step); value = decoded bytes / s; unfused = gather-decompress "
+                              f"then torch.sum per bag",
+                      "slots_host": bag_res["host"], "slots_hbm": bag_res["hbm"]},
         "uncompressed_gather": {
             "zero_copy_host_gbs": round(K * B * 4 * W / (raw_host_ms * 1e-3) / 1e9, 3),
             "hbm_gbs": round(K * B * 4 * W / (raw_hbm_ms * 1e-3) / 1e9, 3)},

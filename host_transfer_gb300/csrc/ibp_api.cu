@@ -553,7 +553,8 @@ int ibp_gather_decompress_bag(const ibp_plan* plan, const uint32_t* slots, uint6
   DeviceGuard g(plan->device);
   if (!g.ok) return IBP_ECUDA;
   const void *dsl, *dbm, *doff, *dout, *dids = nullptr;
-  if (resolve_ptr(slots, plan->device, &dsl) || resolve_ptr(bitmask, plan->device, &dbm) ||
+  int slots_on_device = 1;
+  if (resolve_ptr(slots, plan->device, &dsl, &slots_on_device) || resolve_ptr(bitmask, plan->device, &dbm) ||
       resolve_ptr(bag_offsets, plan->device, &doff) || resolve_ptr(out, plan->device, &dout))
     return IBP_EINVAL;
   if (row_ids && resolve_ptr(row_ids, plan->device, &dids)) return IBP_EINVAL;
@@ -566,6 +567,7 @@ int ibp_gather_decompress_bag(const ibp_plan* plan, const uint32_t* slots, uint6
   d.n_rows = n_rows;
   d.n_out = n_ids;
   d.vec = (plan->W % 4 == 0) && aligned16(d.slots);
+  d.dev_slots = static_cast<uint32_t>(slots_on_device);
   d.rowcap = ((plan->W + 31) / 32) * 32;
   d.pre = prefix_words(plan, d.vec != 0);
   d.G = 1;

@@ -1,0 +1,414 @@
+// ibp_bag.cuh - gather-decompress fused with sum / mean pooling (an
+// "embedding bag"): the rows of each bag are decoded and added into per-lane
+// float accumulators; decoded rows never go to HBM, only one pooled row per
+// bag does.
+//
+// « Résultats »: IBP's rows feed DLRM embedding tables and GNN feature
+// aggregation, whose consumer pools the rows of each bag; « Algorithme
+// central », step 3 (last point): fetching overlaps the logic that consumes
+// the data.  Pooling (the reading, as in the oracle): out[b] = the rows of
+// ids[offsets[b] .. offsets[b+1]) added as IEEE single values in that order
+// from +0.0, or that sum divided by the bag size (mean; an empty bag gives
+// zeros).  A bag with offsets outside 0 <= offsets[b] <= offsets[b+1] <= n_ids
+// gives zeros and IBP_ERANGE; a bad id or a corrupt slot decodes to a zero
+// row that still counts in the bag's size (IBP_ERANGE / IBP_ECORRUPT).
+//
+// The fetch and decode are those of k_decompress_fast (same plan shapes, same
+// three-stage cp.async pipeline of prefix, then rest, per group of G rows).
+// What differs is the unit of work: warp gw owns bags gw, gw + nwarps, ...; a
+// cursor cuts each bag into groups of at most G consecutive ids (a group
+// never spans two bags; an empty or invalid bag is one group of no rows), and
+// the decode of a group adds its rows, in order, into the lanes'
+// accumulators (word lane + 32 s in acc[s]); the group that ends a bag
+// writes the bag's output row.
+#pragma once
+
+#include "ibp_decompress_fast.cuh"
+
+namespace ibp {
+
+template <int R, int SC, int NPL, bool TAB, uint32_t GW>
+__global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
+  using F = FastShape<SC, GW>;
+  using T = TabShape<SC, R, NPL, TAB>;
+  constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
+  constexpr uint32_t EW = TabEntry<R>::EW;
+  constexpr int D = kFastStages;
+  extern __shared__ __align__(128) uint32_t smem[];
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t nw_cta = blockDim.x >> 5;
+  uint32_t* const tab = smem;
+  uint32_t* const epl = smem + T::ENT;
+  uint32_t* const stages = smem + T::WORDS + warp * static_cast<uint32_t>(D) * STAGE;
+  const uint32_t lt = lanemask_lt();
+  const uint32_t lanebit = 1u << lane;
+
+  const PlanView pv = ba.d.pv;
+  const uint32_t* const slots = ba.d.slots;
+  const uint32_t* const bitmask = ba.d.bitmask;
+  const int64_t* const ids = ba.d.ids;
+  const uint32_t p = TAB ? pv.p_min : pv.u_p;
+  const uint32_t pscale = pv.p_scale;
+  const uint32_t bm = pv.u_bm;
+  uint32_t rm[R], rs[R];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    rm[k] = pv.u_rmask[k];
+    rs[k] = pv.u_rsh[k];
+  }
+  if constexpr (TAB) {
+    for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
+      uint32_t* e = tab + w * EW;
+#pragma unroll
+      for (int k = 0; k < (EW == 4 ? 2 : 4); ++k) e[k] = k < R ? __ldg(pv.rmask + k * W + w) : 0u;
+      e[EW == 4 ? 2 : 4] = __ldg(pv.rshift + w);
+      e[EW == 4 ? 3 : 5] = __ldg(pv.bm + w);
+    }
+    if constexpr (NPL > 0) {
+      for (uint32_t i = threadIdx.x; i < SC * NPL; i += blockDim.x)
+        epl[i] = __ldg(pv.eplanes + (i / NPL) * kPlanes + (i % NPL));
+    }
+    __syncthreads();
+  }
+  const bool reuse = (pv.hints & IBP_HINT_ROW_REUSE) != 0;
+  const uint32_t pre = ba.d.pre;  // multiple of 4, <= W
+  const uint32_t pre_ch = pre >> 2;
+  const uint32_t n_rows32 = static_cast<uint32_t>(ba.d.n_rows);  // < 2^31 (checked by the launcher)
+  const uint64_t n_bags = ba.n_bags;
+  const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw_cta + warp;
+  const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw_cta;
+  if (gw >= n_bags) return;  // warp-uniform; only warp-level syncs below
+
+  // ---- the cursor over this warp's bags (warp-uniform state) ----
+  struct Grp {
+    uint64_t bag;  // n_bags: no group
+    uint64_t pos;  // first id position
+    uint32_t n;    // ids in the group (<= G)
+    uint32_t last;  // the group ends its bag
+    uint32_t bad;   // the bag's offsets are invalid
+  };
+  uint64_t cb = gw, cp = 0, ce = 0;
+  uint32_t cbad = 0;
+  auto open_bag = [&]() {
+    const int64_t lo = ba.offsets[cb], hi = ba.offsets[cb + 1];
+    const bool ok = lo >= 0 && lo <= hi && static_cast<uint64_t>(hi) <= ba.n_ids;
+    cp = ok ? static_cast<uint64_t>(lo) : 0;
+    ce = ok ? static_cast<uint64_t>(hi) : 0;
+    cbad = ok ? 0u : 1u;
+  };
+  open_bag();
+  auto next_group = [&]() -> Grp {
+    Grp g{n_bags, 0, 0, 0, 0};
+    if (cb >= n_bags) return g;
+    const uint64_t left = ce - cp;
+    g.bag = cb;
+    g.pos = cp;
+    g.n = static_cast<uint32_t>(left < G ? left : G);
+    g.last = left <= G ? 1u : 0u;
+    g.bad = cbad;
+    cp += g.n;
+    if (g.last) {
+      cb += nwarps;
+      if (cb < n_bags) open_bag();
+    }
+    return g;
+  };
+
+  // Row ids of a group: lane q < n holds the id at position pos + q.
+  constexpr int32_t kNoRow = -1, kBadId = -2;
+  auto load_id = [&](const Grp& g) -> int32_t {
+    if (g.bag >= n_bags || lane >= g.n) return kNoRow;
+    const int64_t id = ids[g.pos + lane];
+    return (id >= 0 && static_cast<uint64_t>(id) < n_rows32) ? static_cast<int32_t>(id) : kBadId;
+  };
+
+  auto issue_prefix = [&](uint32_t* sb, int32_t id, uint32_t& bmw) {
+    if (id >= 0) bmw = ld_u32(bitmask + (static_cast<uint32_t>(id) >> 5));
+#pragma unroll
+    for (uint32_t q = 0; q < G; ++q) {
+      const int32_t idq = __shfl_sync(kAll, id, q);
+      if (idq >= 0) {
+        const uint32_t* src = slots + static_cast<uint64_t>(idq) * W;
+        uint32_t* dst = sb + q * W;
+#pragma unroll
+        for (uint32_t b = 0; b < CB; ++b) {
+          const uint32_t c = lane + 32u * b;
+          if (c < pre_ch) cp_row16(reuse, dst + 4u * c, src + 4u * c);
+        }
+      }
+    }
+  };
+
+  auto row_info = [&](const uint32_t* sb, int32_t id, uint32_t bmw, uint32_t& kind, uint32_t& nt) {
+    kind = kNone;
+    nt = 0;
+    if (id == kNoRow) return;
+    if (id == kBadId) {
+      kind = kBadRange;
+      return;
+    }
+    if (!((bmw >> (static_cast<uint32_t>(id) & 31u)) & 1u)) {
+      kind = kRaw;
+      nt = W;
+      return;
+    }
+    const uint32_t* hb = sb + lane * W;
+    uint32_t m = 0, me = 0;
+    auto count = [&](uint32_t H, uint32_t s) {
+      m += __popc(H);
+      if constexpr (TAB && NPL > 0) {
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) me += __popc(H & epl[s * NPL + k]) << k;
+      }
+    };
+    if constexpr (SC >= 4) {
+#pragma unroll
+      for (uint32_t s = 0; s < SC; s += 4) {
+        const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
+        count(h.x, s);
+        count(h.y, s + 1);
+        count(h.z, s + 2);
+        count(h.w, s + 3);
+      }
+    } else {
+#pragma unroll
+      for (uint32_t s = 0; s < SC; ++s) count(hb[s], s);
+    }
+    const uint32_t Lw = (32u * (SC + W) - p * m - pscale * me + 31u) >> 5;
+    if (Lw >= W) {
+      kind = kCorrupt;
+      return;
+    }
+    kind = kComp;
+    nt = Lw;
+  };
+
+  auto issue_rest = [&](uint32_t* sb, int32_t id, uint32_t kind, uint32_t nt) {
+    const bool need = (kind == kRaw || kind == kComp) && nt > pre;
+    for (uint32_t mk = __ballot_sync(kAll, need); mk; mk &= mk - 1) {
+      const uint32_t q = __ffs(mk) - 1;
+      const uint32_t ntq = __shfl_sync(kAll, nt, q);
+      const uint32_t* src = slots + static_cast<uint64_t>(__shfl_sync(kAll, id, q)) * W;
+      uint32_t* dst = sb + q * W;
+      for (uint32_t c = pre_ch + lane; c < ((ntq + 3u) >> 2); c += 32) cp_row16(reuse, dst + 4u * c, src + 4u * c);
+    }
+  };
+
+  float acc[SC];
+#pragma unroll
+  for (uint32_t s = 0; s < SC; ++s) acc[s] = 0.0f;
+  uint64_t cnt = 0;  // ids of the current bag seen so far
+
+  auto add_row = [&](const uint32_t* pb) {
+    uint32_t base = 32u * SC + 32u * lane;
+    auto seg = [&](uint32_t H, uint32_t s) {
+      uint32_t P = base - p * __popc(H & lt);
+      uint32_t step = 1024u - p * __popc(H);
+      if constexpr (TAB && NPL > 0) {
+        uint32_t e_lt = 0, e_all = 0;
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) {
+          const uint32_t Ek = H & epl[s * NPL + k];
+          e_lt += __popc(Ek & lt) << k;
+          e_all += __popc(Ek) << k;
+        }
+        P -= pscale * e_lt;
+        step -= pscale * e_all;
+      }
+      const uint32_t* q = pb + (P >> 5);
+      const uint32_t v = __funnelshift_r(q[0], q[1], P);
+      uint32_t y;
+      if constexpr (TAB) {
+        const uint32_t* e = tab + (32u * s + lane) * EW;
+        const uint4 e0 = *reinterpret_cast<const uint4*>(e);
+        if constexpr (EW == 4) {
+          const uint32_t m2[2] = {e0.x, e0.y};
+          const uint32_t s2[2] = {e0.z & 0xFFu, (e0.z >> 8) & 0xFFu};
+          y = deposit_runs<(R < 2 ? R : 2)>(v, m2, s2) | e0.w;
+        } else {
+          const uint4 e1 = *reinterpret_cast<const uint4*>(e + 4);
+          const uint32_t m4[4] = {e0.x, e0.y, e0.z, e0.w};
+          const uint32_t s4[4] = {e1.x & 0xFFu, (e1.x >> 8) & 0xFFu, (e1.x >> 16) & 0xFFu, e1.x >> 24};
+          y = deposit_runs<R>(v, m4, s4) | e1.y;
+        }
+      } else {
+        y = deposit_runs<R>(v, rm, rs) | bm;
+      }
+      acc[s] = __fadd_rn(acc[s], __uint_as_float((H & lanebit) ? y : v));
+      base += step;
+    };
+    if constexpr (SC >= 4) {
+#pragma unroll
+      for (uint32_t s = 0; s < SC; s += 4) {
+        const uint4 h = *reinterpret_cast<const uint4*>(pb + s);
+        seg(h.x, s);
+        seg(h.y, s + 1);
+        seg(h.z, s + 2);
+        seg(h.w, s + 3);
+      }
+    } else {
+#pragma unroll
+      for (uint32_t s = 0; s < SC; ++s) seg(pb[s], s);
+    }
+  };
+
+  // Add group g's rows in order; the group that ends a bag writes it out.
+  auto consume = [&](const Grp& g, const uint32_t* sb, uint32_t kind) {
+    const uint32_t comp = __ballot_sync(kAll, kind == kComp);
+    const uint32_t raw = __ballot_sync(kAll, kind == kRaw);
+    const bool bad = kind == kBadRange || kind == kCorrupt;
+    if (bad) record_status(pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
+#pragma unroll
+    for (uint32_t q = 0; q < G; ++q) {
+      if ((comp >> q) & 1u) {
+        add_row(sb + q * W);
+      } else if ((raw >> q) & 1u) {
+#pragma unroll
+        for (uint32_t s = 0; s < SC; ++s) acc[s] = __fadd_rn(acc[s], __uint_as_float(sb[q * W + 32u * s + lane]));
+      }
+    }
+    cnt += g.n;
+    if (g.last) {
+      if (g.bad && lane == 0) record_status(pv.status, IBP_ERANGE);
+      float* const o = ba.out + g.bag * W + lane;
+      const float c = static_cast<float>(cnt);
+#pragma unroll
+      for (uint32_t s = 0; s < SC; ++s) {
+        o[32u * s] = (ba.mean && cnt) ? __fdiv_rn(acc[s], c) : acc[s];
+        acc[s] = 0.0f;
+      }
+      cnt = 0;
+    }
+  };
+
+  // Pipeline over D stages, as in k_decompress_fast: at iteration j, st[k]
+  // holds group j + k; cp.async groups are committed in the order
+  // prefix(j+D-1), rest(j+1), with empty commits in the prologue.
+  Grp gr[D + 1];
+  int32_t idr[D + 1];
+  uint32_t bmr[D];
+  uint32_t* st[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) {
+    gr[i] = next_group();
+    idr[i] = load_id(gr[i]);
+    st[i] = stages + i * STAGE;
+    bmr[i] = 0;
+  }
+#pragma unroll
+  for (int i = 0; i < D - 1; ++i) {
+    issue_prefix(st[i], idr[i], bmr[i]);
+    cp_commit();
+    if (i < D - 2) cp_commit();
+  }
+  cp_wait<2 * D - 4>();
+  __syncwarp();
+  uint32_t kind0, nt0;
+  row_info(st[0], idr[0], bmr[0], kind0, nt0);
+  issue_rest(st[0], idr[0], kind0, nt0);
+  cp_commit();
+
+  while (gr[0].bag < n_bags) {
+    gr[D] = next_group();
+    idr[D] = load_id(gr[D]);
+    issue_prefix(st[D - 1], idr[D - 1], bmr[D - 1]);
+    cp_commit();
+    cp_wait<2 * D - 4>();
+    __syncwarp();
+    uint32_t kind1, nt1;
+    row_info(st[1], idr[1], bmr[1], kind1, nt1);
+    issue_rest(st[1], idr[1], kind1, nt1);
+    cp_commit();
+    cp_wait<2>();
+    __syncwarp();
+    consume(gr[0], st[0], kind0);
+    __syncwarp();
+    kind0 = kind1;
+    uint32_t* const t = st[0];
+#pragma unroll
+    for (int i = 0; i < D - 1; ++i) st[i] = st[i + 1];
+    st[D - 1] = t;
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+      gr[i] = gr[i + 1];
+      idr[i] = idr[i + 1];
+    }
+#pragma unroll
+    for (int i = 0; i < D - 1; ++i) bmr[i] = bmr[i + 1];
+    bmr[D - 1] = 0;
+  }
+  cp_wait<0>();
+}
+
+template <int R, int SC, int NPL, bool TAB, uint32_t GW>
+static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
+  using F = FastShape<SC, GW>;
+  using T = TabShape<SC, R, NPL, TAB>;
+  const size_t per_warp = 4ull * kFastStages * F::STAGE;
+  const size_t fixed = 4ull * T::WORDS;
+  size_t warps = (220ull * 1024 - fixed) / per_warp;
+  if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
+  if (warps < 1) return IBP_EINVAL;
+  const size_t smem = fixed + warps * per_warp;
+  auto kern = k_bag<R, SC, NPL, TAB, GW>;
+  static int occ_cache[64] = {0};
+  const int dev = plan->device;
+  if (dev < 0 || dev >= 64) return IBP_EINVAL;
+  int occ = occ_cache[dev];
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, static_cast<int>(warps * 32), smem);
+    if (e != cudaSuccess || occ < 1) {
+      set_cuda_error(e, "set-up of k_bag");
+      cudaGetLastError();
+      return IBP_ECUDA;
+    }
+    occ_cache[dev] = occ;
+  }
+  const uint64_t need = (a.n_bags + warps - 1) / warps;
+  const uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
+  const unsigned grid = static_cast<unsigned>(need < cap ? need : cap);
+  kern<<<grid, static_cast<unsigned>(warps * 32), smem, stream>>>(a);
+  return check_launch("k_bag");
+}
+
+template <int R, int NPL, bool TAB, uint32_t GW>
+static int launch_bag_sc(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
+  switch (plan->S) {
+    case 1: return launch_bag_t<R, 1, NPL, TAB, GW>(plan, a, stream);
+    case 2: return launch_bag_t<R, 2, NPL, TAB, GW>(plan, a, stream);
+    case 4: return launch_bag_t<R, 4, NPL, TAB, GW>(plan, a, stream);
+    case 8: return launch_bag_t<R, 8, NPL, TAB, GW>(plan, a, stream);
+    default: return launch_bag_t<R, 16, NPL, TAB, GW>(plan, a, stream);
+  }
+}
+
+template <int R, uint32_t GW>
+static int launch_bag_table(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
+  switch (plan->view.npl) {
+    case 0: return launch_bag_sc<R, 0, true, GW>(plan, a, stream);
+    case 1: return launch_bag_sc<R, 1, true, GW>(plan, a, stream);
+    default: return launch_bag_sc<R, 6, true, GW>(plan, a, stream);
+  }
+}
+
+template <uint32_t GW>
+static int launch_bag_gw(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
+  if (!plan->uniform)
+    return plan->max_runs <= 2 ? launch_bag_table<2, GW>(plan, a, stream) : launch_bag_table<4, GW>(plan, a, stream);
+  switch (plan->max_runs) {
+    case 1: return launch_bag_sc<1, 0, false, GW>(plan, a, stream);
+    case 2: return launch_bag_sc<2, 0, false, GW>(plan, a, stream);
+    case 3: return launch_bag_sc<3, 0, false, GW>(plan, a, stream);
+    default: return launch_bag_sc<4, 0, false, GW>(plan, a, stream);
+  }
+}
+
+// Instantiation units (compiled in parallel), one per group size.
+int launch_bag_256(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
+int launch_bag_512(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
+int launch_bag_1024(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
+
+}  // namespace ibp

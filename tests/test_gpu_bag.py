@@ -155,3 +155,23 @@ def test_bag_rejects_bad_arguments():
     empty = ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]), ids,
                                           torch.zeros(1, dtype=torch.int64, device="cuda"))
     assert empty.shape == (0, 64)
+
+
+@pytest.mark.parametrize("W", [32, 64, 128, 512])
+def test_bag_row_reuse_hint_from_host(W):
+    """Row-reuse copies from host-mapped slots take the small-group kernels;
+    results are unchanged."""
+    rng = np.random.default_rng(90 + W)
+    n = max(64, 60_000 // W)
+    rows = _rows(rng, n, W)
+    g = gpu_codec(rows, rows[: n // 2], 0.9, "host")
+    g["plan"].set_hints(ibp.IBP_HINT_ROW_REUSE)
+    hot = rng.integers(0, n, 7)
+    ids = np.where(rng.random(2500) < 0.6, hot[rng.integers(0, 7, 2500)], rng.integers(0, n, 2500)).astype(np.int64)
+    offsets = _bags(rng, len(ids), max(1, 256 // W))
+    for mode in (ibp.IBP_BAG_SUM, ibp.IBP_BAG_MEAN):
+        out = ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]),
+                                            torch.from_numpy(ids).cuda(), torch.from_numpy(offsets).cuda(), mode)
+        assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
+        st, want = _expected(g, ids, offsets, mode)
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), want)
