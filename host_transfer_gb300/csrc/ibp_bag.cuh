@@ -78,7 +78,12 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   const uint64_t n_bags = ba.n_bags;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw_cta + warp;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw_cta;
+  // Programmatic dependent launch, as in k_decompress_fast: the next kernel
+  // may start as this grid drains; wait for the previous grid before
+  // touching per-call data.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (gw >= n_bags) return;  // warp-uniform; only warp-level syncs below
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- the cursor over this warp's bags (warp-uniform state) ----
   struct Grp {
@@ -370,7 +375,22 @@ static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   const uint64_t need = (a.n_bags + warps - 1) / warps;
   const uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
   const unsigned grid = static_cast<unsigned>(need < cap ? need : cap);
-  kern<<<grid, static_cast<unsigned>(warps * 32), smem, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(static_cast<unsigned>(warps * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "k_bag");
+    cudaGetLastError();
+    return IBP_ECUDA;
+  }
   return check_launch("k_bag");
 }
 

@@ -138,7 +138,15 @@ __global__ void __launch_bounds__(kFastWarps * 32, (!TAB && SC <= 32) ? 4 : 1) k
   const uint64_t n_groups = (n_out + G - 1) / G;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw_cta + warp;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw_cta;
+  // Programmatic dependent launch: the next kernel of the stream may start
+  // its CTAs as this grid's CTAs exit (its prologue overlaps this grid's
+  // drain), and every CTA waits for the previous grid to complete, with its
+  // memory visible, before touching per-call data (ids, bitmask, slots,
+  // output, status).  The plan tables read above are written only when the
+  // plan is created.  Without the launch attribute both are no-ops.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (gw >= n_groups) return;  // warp-uniform; only warp-level syncs below
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint64_t J = (n_groups - gw + nwarps - 1) / nwarps;
   const uint64_t row_step = nwarps * G;  // first row of group j+1 minus first row of group j
 
@@ -448,7 +456,22 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
   if (MP) cap = cap / a.n_plans > 0 ? cap / a.n_plans : 1;  // CTAs per plan
   const dim3 grid(static_cast<unsigned>(need < cap ? need : cap), MP ? a.n_plans : 1u);
-  kern<<<grid, static_cast<unsigned>(warps * 32), smem, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(static_cast<unsigned>(warps * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "k_decompress_fast");
+    cudaGetLastError();
+    return IBP_ECUDA;
+  }
   return check_launch("k_decompress_fast");
 }
 
