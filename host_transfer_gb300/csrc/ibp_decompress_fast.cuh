@@ -71,11 +71,20 @@ struct FastShape {
 // MP = true (plan sets, contiguous decode, table path): CTA row blockIdx.y
 // decodes rows [y * rows_per_plan, (y + 1) * rows_per_plan) of the table with
 // plan y of a.plans (a device array of plan views).
-// Uniform plans up to W = 1024 fit four CTAs per SM's registers without
-// spilling (measured: +1 % on dense and DLRM rows); wider or per-word-table
-// shapes would spill under that limit.
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false>
-__global__ void __launch_bounds__(kFastWarps * 32, (!TAB && SC <= 32) ? 4 : 1) k_decompress_fast(const DecodeArgs a) {
+// CTAs per SM the register allocation is sized for, where that causes no
+// spills (measured on one GB300): uniform plans up to W = 1024 fit four (+1 %
+// on dense and DLRM rows); per-word-table plans up to W = 512 with at most one
+// e-plane fit three instead of the two that 107 registers allowed, which pays
+// for slots in device memory (DEV: sparse rows +9 %) but not over the host
+// link (-2 %); other shapes keep the compiler's choice.
+template <int SC, int NPL, bool TAB, bool MP, bool DEV>
+constexpr int fast_min_blocks() {
+  return !TAB ? (SC <= 32 ? 4 : 1) : ((DEV && !MP && SC <= 16 && NPL <= 1) ? 3 : 1);
+}
+
+// DEV only selects the register budget (fast_min_blocks).
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false>
+__global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV>())) k_decompress_fast(const DecodeArgs a) {
   static_assert(!MP || (TAB && !PK), "plan sets decode through the table path, slot layout");
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -423,7 +432,7 @@ __global__ void __launch_bounds__(kFastWarps * 32, (!TAB && SC <= 32) ? 4 : 1) k
   cp_wait<0>();
 }
 
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false>
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false>
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -433,7 +442,7 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = fixed + warps * per_warp;
-  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW, MP>;
+  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW, MP, DEV>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
   // for this launch shape.
   static int occ_cache[64] = {0};
@@ -475,16 +484,16 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   return check_launch("k_decompress_fast");
 }
 
-template <int R, int NPL, bool TAB, bool PK, uint32_t GW>
+template <int R, int NPL, bool TAB, bool PK, uint32_t GW, bool DEV = false>
 static int launch_fast_sc(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   switch (plan->S) {
-    case 1: return launch_fast_t<R, 1, NPL, TAB, PK, GW>(plan, a, stream);
-    case 2: return launch_fast_t<R, 2, NPL, TAB, PK, GW>(plan, a, stream);
-    case 4: return launch_fast_t<R, 4, NPL, TAB, PK, GW>(plan, a, stream);
-    case 8: return launch_fast_t<R, 8, NPL, TAB, PK, GW>(plan, a, stream);
-    case 16: return launch_fast_t<R, 16, NPL, TAB, PK, GW>(plan, a, stream);
-    case 32: return launch_fast_t<R, 32, NPL, TAB, PK, GW>(plan, a, stream);
-    default: return launch_fast_t<R, 64, NPL, TAB, PK, GW>(plan, a, stream);
+    case 1: return launch_fast_t<R, 1, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
+    case 2: return launch_fast_t<R, 2, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
+    case 4: return launch_fast_t<R, 4, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
+    case 8: return launch_fast_t<R, 8, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
+    case 16: return launch_fast_t<R, 16, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
+    case 32: return launch_fast_t<R, 32, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
+    default: return launch_fast_t<R, 64, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
   }
 }
 
@@ -498,19 +507,19 @@ static int launch_fast_uniform_t(const ibp_plan* plan, DecodeArgs& a, cudaStream
   }
 }
 
-template <int R, bool PK, uint32_t GW>
+template <int R, bool PK, uint32_t GW, bool DEV = false>
 static int launch_table_r(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   switch (plan->view.npl) {
-    case 0: return launch_fast_sc<R, 0, true, PK, GW>(plan, a, stream);
-    case 1: return launch_fast_sc<R, 1, true, PK, GW>(plan, a, stream);
-    default: return launch_fast_sc<R, 6, true, PK, GW>(plan, a, stream);
+    case 0: return launch_fast_sc<R, 0, true, PK, GW, DEV>(plan, a, stream);
+    case 1: return launch_fast_sc<R, 1, true, PK, GW, DEV>(plan, a, stream);
+    default: return launch_fast_sc<R, 6, true, PK, GW, DEV>(plan, a, stream);
   }
 }
 
-template <bool PK, uint32_t GW>
+template <bool PK, uint32_t GW, bool DEV = false>
 static int launch_fast_table_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  return plan->max_runs <= 2 ? launch_table_r<2, PK, GW>(plan, a, stream)
-                             : launch_table_r<4, PK, GW>(plan, a, stream);
+  return plan->max_runs <= 2 ? launch_table_r<2, PK, GW, DEV>(plan, a, stream)
+                             : launch_table_r<4, PK, GW, DEV>(plan, a, stream);
 }
 
 template <int R, int NPL>
@@ -531,6 +540,7 @@ static int launch_fast_set_sc(const ibp_plan* plan0, DecodeArgs& a, cudaStream_t
 int launch_fast_uniform(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_uniform_reuse(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_table(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+int launch_fast_table_dev(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_table_reuse(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_uniform_packed(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_table_packed(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
