@@ -76,3 +76,28 @@ def test_a_planted_order_mistake_is_caught():
     fwd = B.embedding_bag(_f(x), np.array([0, 3], np.int64), B.SUM)[1]
     rev = B.embedding_bag(_f(x[::-1].copy()), np.array([0, 3], np.int64), B.SUM)[1]
     assert _vals(fwd)[0, 0] == 0.0 and _vals(rev)[0, 0] == 1.0
+
+
+def test_bf16_rows_widen_exactly_and_pool_per_element():
+    # bf16 1.5 = 0x3FC0, -2.0 = 0xC000, 0.375 = 0x3EC0: exact in both formats
+    w = np.array([[0xC0003FC0], [0x3EC03FC0]], np.uint32)  # rows (1.5, -2.0) and (1.5, 0.375)
+    st, out = B.embedding_bag(w, np.array([0, 2], np.int64), B.SUM, bf16=True)
+    assert st == B.OK and out.shape == (1, 2)
+    assert np.array_equal(out.view(np.float32)[0], [3.0, -1.625])
+    st, m = B.embedding_bag(w, np.array([0, 2], np.int64), B.MEAN, bf16=True)
+    assert np.array_equal(m.view(np.float32)[0], [1.5, -0.8125])
+
+
+def test_bf16_widening_matches_torch_for_every_pattern():
+    """Every bf16 pattern (both halves of a word) widens as torch's own
+    bfloat16 -> float32 conversion does (NaNs compared as NaNs)."""
+    import torch
+
+    h = np.arange(0, 1 << 16, dtype=np.uint32)
+    words = (h | (h[::-1] << 16)).reshape(-1, 1)
+    f = B.bf16_words_to_f32(words)
+    ref = torch.from_numpy(h.astype(np.int32).astype(np.int16)).view(torch.bfloat16).float().numpy()
+    for col, src in ((0, ref), (1, ref[::-1])):
+        nan = np.isnan(src)
+        assert np.array_equal(np.isnan(f[:, col]), nan)
+        assert np.array_equal(f[~nan, col].view(np.uint32), src[~nan].view(np.uint32))
