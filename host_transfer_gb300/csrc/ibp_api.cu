@@ -547,7 +547,8 @@ int ibp_gather_decompress_bag(const ibp_plan* plan, const uint32_t* slots, uint6
   g_detail[0] = 0;
   if (!plan) return IBP_EINVAL;
   if (n_bags == 0) return IBP_OK;
-  if (!slots || !bitmask || !bag_offsets || !out || n_rows == 0 || mode > IBP_BAG_MEAN) return IBP_EINVAL;
+  if (!slots || !bitmask || !bag_offsets || !out || n_rows == 0 || (mode & ~(IBP_BAG_MEAN | IBP_BAG_BF16)))
+    return IBP_EINVAL;
   if ((n_ids > 0 && !row_ids) || n_rows >= (1ull << 31) || n_ids > (1ull << 40) || n_bags > (1ull << 40))
     return IBP_EINVAL;
   DeviceGuard g(plan->device);
@@ -575,7 +576,8 @@ int ibp_gather_decompress_bag(const ibp_plan* plan, const uint32_t* slots, uint6
   a.n_ids = n_ids;
   a.n_bags = n_bags;
   a.out = static_cast<float*>(const_cast<void*>(dout));
-  a.mean = mode;
+  a.mean = (mode & IBP_BAG_MEAN) ? 1u : 0u;
+  a.bf16 = (mode & IBP_BAG_BF16) ? 1u : 0u;
   return launch_bag(plan, a, static_cast<cudaStream_t>(stream));
 }
 

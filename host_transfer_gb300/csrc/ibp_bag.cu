@@ -5,12 +5,14 @@
 // memory to L1, where repeated rows are found), other host-mapped slots 512;
 // slots in device memory take 1024-word groups for W >= 128 (more rows in
 // flight per warp: one bag is one warp's sequence of rows) and 512 below.
+// Rows of bfloat16 pairs take 512-word groups.
 #include "ibp_bag.cuh"
 
 namespace ibp {
 
 int launch_bag(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   if (!fast_decompress_applies(plan, a.d) || plan->S > 16u) return IBP_EINVAL;
+  if (a.bf16) return launch_bag_bf16(plan, a, stream);
   if (!a.d.dev_slots) return (a.d.pv.hints & IBP_HINT_ROW_REUSE) ? launch_bag_256(plan, a, stream)
                                                                    : launch_bag_512(plan, a, stream);
   return plan->W >= 128u ? launch_bag_1024(plan, a, stream) : launch_bag_512(plan, a, stream);

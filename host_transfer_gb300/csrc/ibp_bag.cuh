@@ -27,7 +27,10 @@
 
 namespace ibp {
 
-template <int R, int SC, int NPL, bool TAB, uint32_t GW>
+// BF16: every decoded word holds two bfloat16 elements (element 2j in bits
+// 0-15), each widened exactly to float and pooled on its own; the output row
+// has 2W floats.
+template <int R, int SC, int NPL, bool TAB, uint32_t GW, bool BF16>
 __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -200,10 +203,20 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
     }
   };
 
-  float acc[SC];
+  constexpr uint32_t NA = BF16 ? 2 * SC : SC;  // accumulators per lane
+  float acc[NA];
 #pragma unroll
-  for (uint32_t s = 0; s < SC; ++s) acc[s] = 0.0f;
+  for (uint32_t s = 0; s < NA; ++s) acc[s] = 0.0f;
   uint64_t cnt = 0;  // ids of the current bag seen so far
+  // add decoded word w (word lane + 32 s of a row)
+  auto add_word = [&](uint32_t s, uint32_t w) {
+    if constexpr (BF16) {
+      acc[2 * s] = __fadd_rn(acc[2 * s], __uint_as_float(w << 16));
+      acc[2 * s + 1] = __fadd_rn(acc[2 * s + 1], __uint_as_float(w & 0xFFFF0000u));
+    } else {
+      acc[s] = __fadd_rn(acc[s], __uint_as_float(w));
+    }
+  };
 
   auto add_row = [&](const uint32_t* pb) {
     uint32_t base = 32u * SC + 32u * lane;
@@ -240,7 +253,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
       } else {
         y = deposit_runs<R>(v, rm, rs) | bm;
       }
-      acc[s] = __fadd_rn(acc[s], __uint_as_float((H & lanebit) ? y : v));
+      add_word(s, (H & lanebit) ? y : v);
       base += step;
     };
     if constexpr (SC >= 4) {
@@ -270,19 +283,28 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
         add_row(sb + q * W);
       } else if ((raw >> q) & 1u) {
 #pragma unroll
-        for (uint32_t s = 0; s < SC; ++s) acc[s] = __fadd_rn(acc[s], __uint_as_float(sb[q * W + 32u * s + lane]));
+        for (uint32_t s = 0; s < SC; ++s) add_word(s, sb[q * W + 32u * s + lane]);
       }
     }
     cnt += g.n;
     if (g.last) {
       if (g.bad && lane == 0) record_status(pv.status, IBP_ERANGE);
-      float* const o = ba.out + g.bag * W + lane;
       const float c = static_cast<float>(cnt);
+      const bool div = ba.mean && cnt;
+      if constexpr (BF16) {
+        float2* const o = reinterpret_cast<float2*>(ba.out + g.bag * (2 * W)) + lane;
 #pragma unroll
-      for (uint32_t s = 0; s < SC; ++s) {
-        o[32u * s] = (ba.mean && cnt) ? __fdiv_rn(acc[s], c) : acc[s];
-        acc[s] = 0.0f;
+        for (uint32_t s = 0; s < SC; ++s) {
+          const float lo = acc[2 * s], hi = acc[2 * s + 1];
+          o[32u * s] = div ? make_float2(__fdiv_rn(lo, c), __fdiv_rn(hi, c)) : make_float2(lo, hi);
+        }
+      } else {
+        float* const o = ba.out + g.bag * W + lane;
+#pragma unroll
+        for (uint32_t s = 0; s < SC; ++s) o[32u * s] = div ? __fdiv_rn(acc[s], c) : acc[s];
       }
+#pragma unroll
+      for (uint32_t s = 0; s < NA; ++s) acc[s] = 0.0f;
       cnt = 0;
     }
   };
@@ -346,7 +368,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   cp_wait<0>();
 }
 
-template <int R, int SC, int NPL, bool TAB, uint32_t GW>
+template <int R, int SC, int NPL, bool TAB, uint32_t GW, bool BF16>
 static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -356,7 +378,7 @@ static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = fixed + warps * per_warp;
-  auto kern = k_bag<R, SC, NPL, TAB, GW>;
+  auto kern = k_bag<R, SC, NPL, TAB, GW, BF16>;
   static int occ_cache[64] = {0};
   const int dev = plan->device;
   if (dev < 0 || dev >= 64) return IBP_EINVAL;
@@ -394,35 +416,36 @@ static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   return check_launch("k_bag");
 }
 
-template <int R, int NPL, bool TAB, uint32_t GW>
+template <int R, int NPL, bool TAB, uint32_t GW, bool BF16>
 static int launch_bag_sc(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   switch (plan->S) {
-    case 1: return launch_bag_t<R, 1, NPL, TAB, GW>(plan, a, stream);
-    case 2: return launch_bag_t<R, 2, NPL, TAB, GW>(plan, a, stream);
-    case 4: return launch_bag_t<R, 4, NPL, TAB, GW>(plan, a, stream);
-    case 8: return launch_bag_t<R, 8, NPL, TAB, GW>(plan, a, stream);
-    default: return launch_bag_t<R, 16, NPL, TAB, GW>(plan, a, stream);
+    case 1: return launch_bag_t<R, 1, NPL, TAB, GW, BF16>(plan, a, stream);
+    case 2: return launch_bag_t<R, 2, NPL, TAB, GW, BF16>(plan, a, stream);
+    case 4: return launch_bag_t<R, 4, NPL, TAB, GW, BF16>(plan, a, stream);
+    case 8: return launch_bag_t<R, 8, NPL, TAB, GW, BF16>(plan, a, stream);
+    default: return launch_bag_t<R, 16, NPL, TAB, GW, BF16>(plan, a, stream);
   }
 }
 
-template <int R, uint32_t GW>
+template <int R, uint32_t GW, bool BF16>
 static int launch_bag_table(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   switch (plan->view.npl) {
-    case 0: return launch_bag_sc<R, 0, true, GW>(plan, a, stream);
-    case 1: return launch_bag_sc<R, 1, true, GW>(plan, a, stream);
-    default: return launch_bag_sc<R, 6, true, GW>(plan, a, stream);
+    case 0: return launch_bag_sc<R, 0, true, GW, BF16>(plan, a, stream);
+    case 1: return launch_bag_sc<R, 1, true, GW, BF16>(plan, a, stream);
+    default: return launch_bag_sc<R, 6, true, GW, BF16>(plan, a, stream);
   }
 }
 
-template <uint32_t GW>
+template <uint32_t GW, bool BF16>
 static int launch_bag_gw(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   if (!plan->uniform)
-    return plan->max_runs <= 2 ? launch_bag_table<2, GW>(plan, a, stream) : launch_bag_table<4, GW>(plan, a, stream);
+    return plan->max_runs <= 2 ? launch_bag_table<2, GW, BF16>(plan, a, stream)
+                               : launch_bag_table<4, GW, BF16>(plan, a, stream);
   switch (plan->max_runs) {
-    case 1: return launch_bag_sc<1, 0, false, GW>(plan, a, stream);
-    case 2: return launch_bag_sc<2, 0, false, GW>(plan, a, stream);
-    case 3: return launch_bag_sc<3, 0, false, GW>(plan, a, stream);
-    default: return launch_bag_sc<4, 0, false, GW>(plan, a, stream);
+    case 1: return launch_bag_sc<1, 0, false, GW, BF16>(plan, a, stream);
+    case 2: return launch_bag_sc<2, 0, false, GW, BF16>(plan, a, stream);
+    case 3: return launch_bag_sc<3, 0, false, GW, BF16>(plan, a, stream);
+    default: return launch_bag_sc<4, 0, false, GW, BF16>(plan, a, stream);
   }
 }
 
@@ -430,5 +453,6 @@ static int launch_bag_gw(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) 
 int launch_bag_256(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
 int launch_bag_512(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
 int launch_bag_1024(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
+int launch_bag_bf16(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);  // 512-word groups
 
 }  // namespace ibp

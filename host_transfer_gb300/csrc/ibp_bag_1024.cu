@@ -5,7 +5,7 @@
 namespace ibp {
 
 int launch_bag_1024(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
-  return launch_bag_gw<1024u>(plan, a, stream);
+  return launch_bag_gw<1024u, false>(plan, a, stream);
 }
 
 }  // namespace ibp

@@ -5,7 +5,7 @@
 namespace ibp {
 
 int launch_bag_256(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
-  return launch_bag_gw<256u>(plan, a, stream);
+  return launch_bag_gw<256u, false>(plan, a, stream);
 }
 
 }  // namespace ibp

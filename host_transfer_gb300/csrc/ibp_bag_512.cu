@@ -5,7 +5,7 @@
 namespace ibp {
 
 int launch_bag_512(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
-  return launch_bag_gw<512u>(plan, a, stream);
+  return launch_bag_gw<512u, false>(plan, a, stream);
 }
 
 }  // namespace ibp

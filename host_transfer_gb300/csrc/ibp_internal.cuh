@@ -131,6 +131,7 @@ struct BagArgs {
   uint64_t n_bags;
   float* out;              // n_bags x W
   uint32_t mean;           // 0: sum, 1: mean
+  uint32_t bf16;           // rows of bfloat16 pairs: out has 2W floats per bag
 };
 // Specialised shapes only (as fast_decompress_applies, S <= 16); else IBP_EINVAL.
 int launch_bag(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);

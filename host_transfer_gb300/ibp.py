@@ -338,14 +338,16 @@ def ibp_row_lengths(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_
 
 IBP_BAG_SUM = 0
 IBP_BAG_MEAN = 1
+IBP_BAG_BF16 = 2
 
 
 def ibp_gather_decompress_bag(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_ids: torch.Tensor,
                               bag_offsets: torch.Tensor, mode: int = IBP_BAG_SUM,
                               out: torch.Tensor | None = None, stream=None,
                               n_rows: int | None = None) -> torch.Tensor:
-    """Pooled rows per bag (float32 device tensor [n_bags, W]) of the rows
-    row_ids[bag_offsets[b] .. bag_offsets[b+1])."""
+    """Pooled rows per bag (float32 device tensor [n_bags, W], or [n_bags, 2W]
+    with IBP_BAG_BF16 in mode) of the rows row_ids[bag_offsets[b] ..
+    bag_offsets[b+1])."""
     lib = load()
     sp, n, W = _word_rows(slots)
     if W != plan.W:
@@ -356,7 +358,8 @@ def ibp_gather_decompress_bag(plan: Plan, slots: torch.Tensor, bitmask: torch.Te
     n_bags = bag_offsets.numel() - 1
     dev = torch.device("cuda", plan.device)
     if out is None:
-        out = torch.empty((max(n_bags, 0), W), dtype=torch.float32, device=dev)
+        width = 2 * W if int(mode) & IBP_BAG_BF16 else W
+        out = torch.empty((max(n_bags, 0), width), dtype=torch.float32, device=dev)
     if n_bags <= 0:
         return out
     with torch.cuda.device(dev):

@@ -337,6 +337,9 @@ int ibp_gather_decompress_packed(const ibp_plan* plan, const uint32_t* packed,
  * multiply-add): bit-identical to gather-decompress followed by that loop.
  * IBP_BAG_MEAN: that sum divided by the bag size (one correctly rounded
  * division); an empty bag gives zeros in both modes.
+ * IBP_BAG_BF16 (or-ed into mode): the rows hold 2W bfloat16 values, word j
+ * holding element 2j in bits 0-15 and 2j+1 in bits 16-31; each is widened
+ * exactly to float and pooled as above, and out holds 2W floats per bag.
  *
  * slots, bitmask, n_rows  as for ibp_gather_decompress; W = 32 * 2^k <= 512,
  *                 at most 4 runs of kept bits per word, slots 16-byte aligned,
@@ -345,13 +348,15 @@ int ibp_gather_decompress_packed(const ibp_plan* plan, const uint32_t* packed,
  * bag_offsets device-accessible int64[n_bags + 1].  A bag whose offsets are
  *             not 0 <= bag_offsets[b] <= bag_offsets[b+1] <= n_ids gives zeros
  *             and records IBP_ERANGE.
- * out         device-accessible float[n_bags * W].
+ * out         device-accessible float[n_bags * W] (n_bags * 2W with IBP_BAG_BF16;
+ *             8-byte aligned then).
  * Data errors as in ibp_gather_decompress: a bad id or a corrupt slot adds a
  * zero row (it still counts in the bag's size) and records IBP_ERANGE /
  * IBP_ECORRUPT.  Asynchronous on `stream`.  Errors: IBP_EINVAL, IBP_ECUDA.
  */
 #define IBP_BAG_SUM 0u
 #define IBP_BAG_MEAN 1u
+#define IBP_BAG_BF16 2u
 int ibp_gather_decompress_bag(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
                               const uint32_t* bitmask, const int64_t* row_ids, uint64_t n_ids,
                               const int64_t* bag_offsets, uint64_t n_bags, uint32_t mode, float* out,

@@ -151,7 +151,7 @@ def test_bag_rejects_bad_arguments():
     rows = _rows(rng, 64, 64)
     g = gpu_codec(rows, rows, 0.9, "hbm")
     with pytest.raises(ibp.IbpError):
-        ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]), ids, off, mode=2)
+        ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]), ids, off, mode=4)
     empty = ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]), ids,
                                           torch.zeros(1, dtype=torch.int64, device="cuda"))
     assert empty.shape == (0, 64)
@@ -174,4 +174,34 @@ def test_bag_row_reuse_hint_from_host(W):
                                             torch.from_numpy(ids).cuda(), torch.from_numpy(offsets).cuda(), mode)
         assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
         st, want = _expected(g, ids, offsets, mode)
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), want)
+
+
+def _bf16_rows(rng, n, W):
+    """Rows of 2W bfloat16 values (N(0, 0.5), every 9th row N(0, 1e3)) as W
+    words of pairs."""
+    from host_transfer_gb300 import workloads
+
+    x = rng.normal(0, 0.5, (n, 2 * W))
+    x[::9] = rng.normal(0, 1e3, (len(x[::9]), 2 * W))
+    return workloads.bf16_pairs_to_words(workloads.f32_to_bf16_bits(x.astype(np.float32)))
+
+
+@pytest.mark.parametrize("W", [32, 64, 128, 512])
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_bag_bf16_rows_match_oracle(W, where):
+    rng = np.random.default_rng(300 + W)
+    n = max(64, 60_000 // W)
+    rows = _bf16_rows(rng, n, W)
+    g = gpu_codec(rows, np.delete(rows, np.s_[::9], axis=0), 0.9, where)
+    ids = rng.integers(0, n, 2500).astype(np.int64)
+    offsets = _bags(rng, len(ids), max(1, 512 // W))
+    for mode in (ibp.IBP_BAG_SUM, ibp.IBP_BAG_MEAN):
+        out = ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]),
+                                            torch.from_numpy(ids).cuda(), torch.from_numpy(offsets).cuda(),
+                                            mode | ibp.IBP_BAG_BF16)
+        assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
+        assert out.shape == (len(offsets) - 1, 2 * W)
+        st, dec = C.decompress(words_np(g["slots_t"]), g["bitmask"], ids, g["mask"], g["bitval"])
+        _, want = B.embedding_bag(dec, offsets, mode, bf16=True)
         assert np.array_equal(out.cpu().numpy().view(np.uint32), want)
