@@ -43,7 +43,11 @@
  *   tables and one status word.  No call allocates on the decompress path.
  * - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
  *   Calls other than ibp_plan_create / ibp_plan_destroy / ibp_get_status are
- *   asynchronous with respect to the host and ordered on `stream`.
+ *   asynchronous with respect to the host and ordered on `stream`.  The
+ *   decompress kernels are launched as programmatic dependents: their blocks
+ *   may be placed on the GPU while the previous kernel of the stream drains,
+ *   but they read and write no per-call data (ids, slots, bitmask, outputs,
+ *   status) before that kernel has completed, so stream order holds.
  * - Alignment: slots, rows and outputs whose base is 16-byte aligned and whose
  *   W is a multiple of 4 take the 16-byte vector path; anything else takes a
  *   4-byte path with identical results.
@@ -59,7 +63,7 @@
 extern "C" {
 #endif
 
-#define IBP_VERSION 1
+#define IBP_VERSION 2
 #define IBP_MAX_W 8192u
 #define IBP_NOALLOC_MAX_W 4096u
 
