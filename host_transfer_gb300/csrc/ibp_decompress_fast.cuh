@@ -342,9 +342,18 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     const uint32_t raw = __ballot_sync(kAll, kind == kRaw);
     const bool bad = kind == kBadRange || kind == kCorrupt;
     const uint32_t badm = __ballot_sync(kAll, bad);
+    constexpr uint32_t kGroupBits = G >= 32 ? kAll : (1u << G) - 1u;
+    if (!TAB && comp == kGroupBits) {
+      // uniform plan, every row compressed (the common case): straight-line
+      // code, so the rows' independent offset chains and shared loads can
+      // overlap
 #pragma unroll
-    for (uint32_t q = 0; q < G; ++q) {
-      if ((comp >> q) & 1u) decode_row(sb + q * W, obase + q * W);
+      for (uint32_t q = 0; q < G; ++q) decode_row(sb + q * W, obase + q * W);
+    } else {
+#pragma unroll
+      for (uint32_t q = 0; q < G; ++q) {
+        if ((comp >> q) & 1u) decode_row(sb + q * W, obase + q * W);
+      }
     }
     if (raw | badm) {
       if (bad) record_status(pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
