@@ -479,11 +479,14 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   cfg.blockDim = dim3(static_cast<unsigned>(warps * 32));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  // Programmatic dependent launch only for a grid that fills the GPU: with
+  // fewer CTAs than it holds, the next launches' CTAs would be placed at once
+  // and wait there, grid after grid (a small grid measured 1.6x slower).
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = grid.x * grid.y >= cap * (MP ? a.n_plans : 1u) ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) {
     set_cuda_error(e, "k_decompress_fast");
