@@ -171,6 +171,13 @@ int ibp_plan_create(const uint32_t* mask, const uint32_t* bitval, uint32_t W, in
     delete p;
     return IBP_ENOMEM;
   }
+  e = cudaHostAlloc(reinterpret_cast<void**>(&p->h_status), 4, cudaHostAllocDefault);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(p->d_block);
+    delete p;
+    return IBP_ENOMEM;
+  }
   uint32_t* base = static_cast<uint32_t*>(p->d_block);
   PlanView& v = p->view;
   v.W = W;
@@ -192,12 +199,14 @@ int ibp_plan_create(const uint32_t* mask, const uint32_t* bitval, uint32_t W, in
     set_cuda_error(e, "ibp_plan_create copy");
     cudaGetLastError();
     cudaFree(p->d_block);
+    cudaFreeHost(p->h_status);
     delete p;
     return IBP_ECUDA;
   }
   int rc = build_plan_tables(p);
   if (rc != IBP_OK) {
     cudaFree(p->d_block);
+    cudaFreeHost(p->h_status);
     delete p;
     return rc;
   }
@@ -209,6 +218,8 @@ int ibp_plan_destroy(ibp_plan* plan) {
   if (!plan) return IBP_OK;
   DeviceGuard g(plan->device);
   cudaError_t e = cudaFree(plan->d_block);
+  const cudaError_t e2 = cudaFreeHost(plan->h_status);
+  if (e == cudaSuccess) e = e2;
   delete plan;
   if (e != cudaSuccess) {
     set_cuda_error(e, "cudaFree");
@@ -484,10 +495,15 @@ int ibp_get_status(const ibp_plan* plan, void* stream) {
   if (!plan) return IBP_EINVAL;
   DeviceGuard g(plan->device);
   if (!g.ok) return IBP_ECUDA;
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-  uint32_t st = 0;
-  if (e == cudaSuccess) e = cudaMemcpy(&st, plan->view.status, 4, cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess && st != 0) e = cudaMemset(plan->view.status, 0, 4);
+  // one copy into the plan's pinned word, ordered on the stream, then one wait
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(plan->h_status, plan->view.status, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  const uint32_t st = e == cudaSuccess ? *plan->h_status : 0u;
+  if (e == cudaSuccess && st != 0) {
+    e = cudaMemsetAsync(plan->view.status, 0, 4, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
   if (e != cudaSuccess) {
     set_cuda_error(e, "ibp_get_status");
     cudaGetLastError();

@@ -72,6 +72,7 @@ struct ibp_plan {
   uint32_t lmin;  // min(W, words of the shortest possible compressed stream)
   uint32_t prefix;  // words fetched before the headers (slot layout); 0 = from lmin
   void* d_block;  // single device allocation holding every table + status
+  uint32_t* h_status;  // pinned host word the status is read back into
   size_t d_bytes;
   ibp::PlanView view;
 };
