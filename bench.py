@@ -165,7 +165,8 @@ def measured_peaks() -> dict:
 
 KERNEL_SOURCES = ["ibp_decompress_fast.cuh", "ibp_decompress_fast_u.cu", "ibp_decompress_fast_t.cu",
                   "ibp_decompress_fast_up.cu", "ibp_decompress_fast_tp.cu", "ibp_decompress_fast_ur.cu",
-                  "ibp_decompress_fast_tr.cu", "ibp_decompress_fast_td.cu", "ibp_decompress_fast_set.cu",
+                  "ibp_decompress_fast_tr.cu", "ibp_decompress_fast_td.cu", "ibp_decompress_fast_ud.cu",
+                  "ibp_decompress_fast_set.cu",
                   "ibp_decompress.cu", "ibp_internal.cuh", "ibp_api.cu"]
 
 

@@ -39,6 +39,11 @@ constexpr uint32_t kAll = 0xFFFFFFFFu;
 // memory to L1, which is where repeated rows are found.
 constexpr uint32_t kGroupWords = 512;
 constexpr uint32_t kGroupWordsReuse = 256;
+// Slots in device memory (measured): uniform plans take 768-word groups (dense
+// HBM 2395 -> 2580 GB/s: longer straight-line decode blocks), per-word-table
+// plans 1024 (sparse HBM 2167 -> 2299 GB/s: two 512-word rows per group).
+constexpr uint32_t kGroupWordsDev = 768;
+constexpr uint32_t kGroupWordsDevTable = 1024;
 
 // Words of a per-word table entry in shared memory: {run masks, packed run
 // shifts, Bitval & Mask}: 4 words for up to two runs, 8 for up to four.
@@ -72,19 +77,24 @@ struct FastShape {
 // decodes rows [y * rows_per_plan, (y + 1) * rows_per_plan) of the table with
 // plan y of a.plans (a device array of plan views).
 // CTAs per SM the register allocation is sized for, where that causes no
-// spills (measured on one GB300): uniform plans up to W = 1024 fit four (+1 %
-// on dense and DLRM rows); per-word-table plans up to W = 512 with at most one
-// e-plane fit three instead of the two that 107 registers allowed, which pays
-// for slots in device memory (DEV: sparse rows +9 %) but not over the host
-// link (-2 %); other shapes keep the compiler's choice.
-template <int SC, int NPL, bool TAB, bool MP, bool DEV>
+// spills (measured on one GB300): uniform plans up to W = 1024 with 512-word
+// groups fit four (+1 % on dense and DLRM rows); with the larger groups of
+// device slots shared memory holds two, and a two-CTA budget leaves the
+// straight-line decode its registers; per-word-table plans up to W = 512 with
+// at most one e-plane fit three with 512-word groups (instead of the two that
+// 107 registers allowed: +9 % for device slots, -2 % over the host link, so
+// host slots keep the compiler's choice) and two with 1024-word groups; other
+// shapes keep the compiler's choice.
+template <int SC, int NPL, bool TAB, bool MP, bool DEV, uint32_t GW>
 constexpr int fast_min_blocks() {
-  return !TAB ? (SC <= 32 ? 4 : 1) : ((DEV && !MP && SC <= 16 && NPL <= 1) ? 3 : 1);
+  if (!TAB) return DEV ? 2 : (SC <= 32 ? 4 : 1);
+  if (DEV && !MP && SC <= 16 && NPL <= 1) return GW >= 1024 ? 2 : 3;
+  return 1;
 }
 
 // DEV only selects the register budget (fast_min_blocks).
 template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false>
-__global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV>())) k_decompress_fast(const DecodeArgs a) {
+__global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV, GW>())) k_decompress_fast(const DecodeArgs a) {
   static_assert(!MP || (TAB && !PK), "plan sets decode through the table path, slot layout");
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -509,13 +519,13 @@ static int launch_fast_sc(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stre
   }
 }
 
-template <bool PK, uint32_t GW>
+template <bool PK, uint32_t GW, bool DEV = false>
 static int launch_fast_uniform_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   switch (plan->max_runs) {
-    case 1: return launch_fast_sc<1, 0, false, PK, GW>(plan, a, stream);
-    case 2: return launch_fast_sc<2, 0, false, PK, GW>(plan, a, stream);
-    case 3: return launch_fast_sc<3, 0, false, PK, GW>(plan, a, stream);
-    default: return launch_fast_sc<4, 0, false, PK, GW>(plan, a, stream);
+    case 1: return launch_fast_sc<1, 0, false, PK, GW, DEV>(plan, a, stream);
+    case 2: return launch_fast_sc<2, 0, false, PK, GW, DEV>(plan, a, stream);
+    case 3: return launch_fast_sc<3, 0, false, PK, GW, DEV>(plan, a, stream);
+    default: return launch_fast_sc<4, 0, false, PK, GW, DEV>(plan, a, stream);
   }
 }
 
@@ -547,9 +557,11 @@ static int launch_fast_set_sc(const ibp_plan* plan0, DecodeArgs& a, cudaStream_t
 }
 
 // One translation unit each (compiled in parallel): slot layout uniform and
-// table plans with kGroupWords and with kGroupWordsReuse, packed layout
-// uniform and table plans (kGroupWords).
+// table plans on host slots (kGroupWords) and on device slots
+// (kGroupWordsDev, kGroupWordsDevTable), with the row-reuse hint
+// (kGroupWordsReuse), packed layout uniform (device setting) and table plans.
 int launch_fast_uniform(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
+int launch_fast_uniform_dev(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_uniform_reuse(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_table(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);
 int launch_fast_table_dev(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream);

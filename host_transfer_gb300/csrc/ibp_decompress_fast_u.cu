@@ -25,7 +25,7 @@ int launch_decompress_fast(const ibp_plan* plan, DecodeArgs& a, cudaStream_t str
                          : launch_fast_table_packed(plan, a, stream);
   if ((a.pv.hints & IBP_HINT_ROW_REUSE) && !a.dev_slots)
     return plan->uniform ? launch_fast_uniform_reuse(plan, a, stream) : launch_fast_table_reuse(plan, a, stream);
-  if (plan->uniform) return launch_fast_uniform(plan, a, stream);
+  if (plan->uniform) return a.dev_slots ? launch_fast_uniform_dev(plan, a, stream) : launch_fast_uniform(plan, a, stream);
   return a.dev_slots ? launch_fast_table_dev(plan, a, stream) : launch_fast_table(plan, a, stream);
 }
 
