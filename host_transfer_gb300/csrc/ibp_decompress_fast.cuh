@@ -317,13 +317,11 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
         const uint4 e0 = *reinterpret_cast<const uint4*>(e);
         if constexpr (EW == 4) {
           const uint32_t m2[2] = {e0.x, e0.y};
-          const uint32_t s2[2] = {e0.z & 0xFFu, (e0.z >> 8) & 0xFFu};
-          y = deposit_runs<(R < 2 ? R : 2)>(v, m2, s2) | e0.w;
+          y = deposit_runs_packed<(R < 2 ? R : 2)>(v, m2, e0.z) | e0.w;
         } else {
           const uint4 e1 = *reinterpret_cast<const uint4*>(e + 4);
           const uint32_t m4[4] = {e0.x, e0.y, e0.z, e0.w};
-          const uint32_t s4[4] = {e1.x & 0xFFu, (e1.x >> 8) & 0xFFu, (e1.x >> 16) & 0xFFu, e1.x >> 24};
-          y = deposit_runs<R>(v, m4, s4) | e1.y;
+          y = deposit_runs_packed<R>(v, m4, e1.x) | e1.y;
         }
       } else {
         y = deposit_runs<R>(v, rm, rs) | bm;

@@ -255,6 +255,19 @@ __device__ __forceinline__ uint32_t deposit_runs(uint32_t v, const uint32_t* rm,
   return y;
 }
 
+// deposit_runs with the shifts packed one per byte (byte k = shift of run
+// k).  A 32-bit rotate uses only the low 5 bits of its count, so no byte
+// needs masking out; under the run's mask the rotate equals the shift: bits
+// that wrap around land below the run (its shift is at most its position),
+// and the field's garbage above its kept bits lands outside the run.
+template <int R>
+__device__ __forceinline__ uint32_t deposit_runs_packed(uint32_t v, const uint32_t* rm, uint32_t shifts) {
+  uint32_t y = 0;
+#pragma unroll
+  for (int k = 0; k < R; ++k) y |= __funnelshift_l(v, v, shifts >> (8 * k)) & rm[k];
+  return y;
+}
+
 // Inverse of deposit_runs: gather the kept bits of x to the low bits.
 template <int R>
 __device__ __forceinline__ uint32_t extract_runs(uint32_t x, const uint32_t* rm, const uint32_t* rs) {
