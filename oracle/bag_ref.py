@@ -73,9 +73,10 @@ def embedding_bag(decoded: np.ndarray, offsets: np.ndarray, mode: int, bf16: boo
             status = status or ERANGE
             continue
         acc = np.zeros(W, np.float32)  # +0.0
-        for k in range(lo, hi):
-            acc = acc + vals[k]  # elementwise IEEE single additions, in order of k
-        if mode == MEAN and hi > lo:
-            acc = acc / np.float32(hi - lo)
+        with np.errstate(over="ignore", invalid="ignore"):  # IEEE overflow / NaN are results, not errors
+            for k in range(lo, hi):
+                acc = acc + vals[k]  # elementwise IEEE single additions, in order of k
+            if mode == MEAN and hi > lo:
+                acc = acc / np.float32(hi - lo)
         out[b] = acc
     return status, out.view(np.uint32)
