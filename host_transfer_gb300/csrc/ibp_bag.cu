@@ -5,7 +5,8 @@
 // memory to L1, where repeated rows are found), other host-mapped slots 512;
 // slots in device memory take 1024-word groups for W >= 128 (more rows in
 // flight per warp: one bag is one warp's sequence of rows) and 512 below.
-// Rows of bfloat16 pairs take 512-word groups.
+// Rows of bfloat16 pairs take 512-word groups.  Few bags on device slots are
+// pooled by teams of 2 or 4 warps per bag (column split).
 #include "ibp_bag.cuh"
 
 namespace ibp {
@@ -15,7 +16,14 @@ int launch_bag(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   if (a.bf16) return launch_bag_bf16(plan, a, stream);
   if (!a.d.dev_slots) return (a.d.pv.hints & IBP_HINT_ROW_REUSE) ? launch_bag_256(plan, a, stream)
                                                                    : launch_bag_512(plan, a, stream);
-  return plan->W >= 128u ? launch_bag_1024(plan, a, stream) : launch_bag_512(plan, a, stream);
+  if (plan->W < 128u) return launch_bag_512(plan, a, stream);
+  // Few bags: a team of warps per bag, each pooling a slice of the segments,
+  // while the bags leave the GPU's warp slots free (two CTAs of eight warps
+  // per SM with these groups).
+  const uint64_t slots_free = 16ull * sm_count(plan->device);
+  if (plan->S >= 4 && 4 * a.n_bags <= slots_free) return launch_bag_1024_split(plan, a, stream, 4);
+  if (plan->S >= 2 && 2 * a.n_bags <= slots_free) return launch_bag_1024_split(plan, a, stream, 2);
+  return launch_bag_1024(plan, a, stream);
 }
 
 }  // namespace ibp

@@ -30,8 +30,14 @@ namespace ibp {
 // BF16: every decoded word holds two bfloat16 elements (element 2j in bits
 // 0-15), each widened exactly to float and pooled on its own; the output row
 // has 2W floats.
-template <int R, int SC, int NPL, bool TAB, uint32_t GW, bool BF16>
+// CS > 1 (column split, for few bags on device slots): a team of CS
+// consecutive warps takes each bag; all of them fetch its rows (the repeats
+// are L2 hits) and warp `part` of the team decodes and pools only segments
+// [part * SC/CS, (part + 1) * SC/CS), skipping the earlier segments' fields by
+// their headers.  Each column is still added in bag order.
+template <int R, int SC, int NPL, bool TAB, uint32_t GW, bool BF16, int CS = 1>
 __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
+  static_assert(CS >= 1 && SC % CS == 0, "a warp pools whole segments");
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
   constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
@@ -85,7 +91,10 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   // may start as this grid drains; wait for the previous grid before
   // touching per-call data.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (gw >= n_bags) return;  // warp-uniform; only warp-level syncs below
+  constexpr uint32_t SPW = SC / CS;  // segments this warp pools
+  const uint64_t team = gw / CS, nteams = nwarps / CS;  // warps per CTA are a multiple of CS
+  const uint32_t s_lo = CS == 1 ? 0u : static_cast<uint32_t>(gw % CS) * SPW;
+  if (team >= n_bags) return;  // warp-uniform; only warp-level syncs below
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- the cursor over this warp's bags (warp-uniform state) ----
@@ -96,7 +105,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
     uint32_t last;  // the group ends its bag
     uint32_t bad;   // the bag's offsets are invalid
   };
-  uint64_t cb = gw, cp = 0, ce = 0;
+  uint64_t cb = team, cp = 0, ce = 0;
   uint32_t cbad = 0;
   auto open_bag = [&]() {
     const int64_t lo = ba.offsets[cb], hi = ba.offsets[cb + 1];
@@ -117,7 +126,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
     g.bad = cbad;
     cp += g.n;
     if (g.last) {
-      cb += nwarps;
+      cb += nteams;
       if (cb < n_bags) open_bag();
     }
     return g;
@@ -203,12 +212,12 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
     }
   };
 
-  constexpr uint32_t NA = BF16 ? 2 * SC : SC;  // accumulators per lane
+  constexpr uint32_t NA = BF16 ? 2 * SPW : SPW;  // accumulators per lane
   float acc[NA];
 #pragma unroll
   for (uint32_t s = 0; s < NA; ++s) acc[s] = 0.0f;
   uint64_t cnt = 0;  // ids of the current bag seen so far
-  // add decoded word w (word lane + 32 s of a row)
+  // add decoded word w (word lane + 32 (s_lo + s) of a row)
   auto add_word = [&](uint32_t s, uint32_t w) {
     if constexpr (BF16) {
       acc[2 * s] = __fadd_rn(acc[2 * s], __uint_as_float(w << 16));
@@ -220,7 +229,8 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
 
   auto add_row = [&](const uint32_t* pb) {
     uint32_t base = 32u * SC + 32u * lane;
-    auto seg = [&](uint32_t H, uint32_t s) {
+    // segment s of the row, pooled into accumulator j
+    auto seg = [&](uint32_t H, uint32_t s, uint32_t j) {
       uint32_t P = base - p * __popc(H & lt);
       uint32_t step = 1024u - p * __popc(H);
       if constexpr (TAB && NPL > 0) {
@@ -251,21 +261,36 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
       } else {
         y = deposit_runs<R>(v, rm, rs) | bm;
       }
-      add_word(s, (H & lanebit) ? y : v);
+      add_word(j, (H & lanebit) ? y : v);
       base += step;
     };
-    if constexpr (SC >= 4) {
+    if constexpr (CS > 1) {
+      // step over the fields of the segments before this warp's slice
+      for (uint32_t s = 0; s < s_lo; ++s) {
+        const uint32_t H = pb[s];
+        uint32_t step = 1024u - p * __popc(H);
+        if constexpr (TAB && NPL > 0) {
+          uint32_t e_all = 0;
+#pragma unroll
+          for (int k = 0; k < NPL; ++k) e_all += __popc(H & epl[s * NPL + k]) << k;
+          step -= pscale * e_all;
+        }
+        base += step;
+      }
+#pragma unroll
+      for (uint32_t j = 0; j < SPW; ++j) seg(pb[s_lo + j], s_lo + j, j);
+    } else if constexpr (SC >= 4) {
 #pragma unroll
       for (uint32_t s = 0; s < SC; s += 4) {
         const uint4 h = *reinterpret_cast<const uint4*>(pb + s);
-        seg(h.x, s);
-        seg(h.y, s + 1);
-        seg(h.z, s + 2);
-        seg(h.w, s + 3);
+        seg(h.x, s, s);
+        seg(h.y, s + 1, s + 1);
+        seg(h.z, s + 2, s + 2);
+        seg(h.w, s + 3, s + 3);
       }
     } else {
 #pragma unroll
-      for (uint32_t s = 0; s < SC; ++s) seg(pb[s], s);
+      for (uint32_t s = 0; s < SC; ++s) seg(pb[s], s, s);
     }
   };
 
@@ -288,7 +313,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
           add_row(sb + q * W);
         } else if ((raw >> q) & 1u) {
 #pragma unroll
-          for (uint32_t s = 0; s < SC; ++s) add_word(s, sb[q * W + 32u * s + lane]);
+          for (uint32_t j = 0; j < SPW; ++j) add_word(j, sb[q * W + 32u * (s_lo + j) + lane]);
         }
       }
     }
@@ -298,16 +323,16 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
       const float c = static_cast<float>(cnt);
       const bool div = ba.mean && cnt;
       if constexpr (BF16) {
-        float2* const o = reinterpret_cast<float2*>(ba.out + g.bag * (2 * W)) + lane;
+        float2* const o = reinterpret_cast<float2*>(ba.out + g.bag * (2 * W)) + lane + 32u * s_lo;
 #pragma unroll
-        for (uint32_t s = 0; s < SC; ++s) {
-          const float lo = acc[2 * s], hi = acc[2 * s + 1];
-          o[32u * s] = div ? make_float2(__fdiv_rn(lo, c), __fdiv_rn(hi, c)) : make_float2(lo, hi);
+        for (uint32_t j = 0; j < SPW; ++j) {
+          const float lo = acc[2 * j], hi = acc[2 * j + 1];
+          o[32u * j] = div ? make_float2(__fdiv_rn(lo, c), __fdiv_rn(hi, c)) : make_float2(lo, hi);
         }
       } else {
-        float* const o = ba.out + g.bag * W + lane;
+        float* const o = ba.out + g.bag * W + lane + 32u * s_lo;
 #pragma unroll
-        for (uint32_t s = 0; s < SC; ++s) o[32u * s] = div ? __fdiv_rn(acc[s], c) : acc[s];
+        for (uint32_t j = 0; j < SPW; ++j) o[32u * j] = div ? __fdiv_rn(acc[j], c) : acc[j];
       }
 #pragma unroll
       for (uint32_t s = 0; s < NA; ++s) acc[s] = 0.0f;
@@ -374,7 +399,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   cp_wait<0>();
 }
 
-template <int R, int SC, int NPL, bool TAB, uint32_t GW, bool BF16>
+template <int R, int SC, int NPL, bool TAB, uint32_t GW, bool BF16, int CS = 1>
 static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   using F = FastShape<SC, GW>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -384,7 +409,8 @@ static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = fixed + warps * per_warp;
-  auto kern = k_bag<R, SC, NPL, TAB, GW, BF16>;
+  if (warps % CS != 0) return IBP_EINVAL;  // a team's warps share a CTA
+  auto kern = k_bag<R, SC, NPL, TAB, GW, BF16, CS>;
   static int occ_cache[64] = {0};
   const int dev = plan->device;
   if (dev < 0 || dev >= 64) return IBP_EINVAL;
@@ -400,7 +426,7 @@ static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
     }
     occ_cache[dev] = occ;
   }
-  const uint64_t need = (a.n_bags + warps - 1) / warps;
+  const uint64_t need = (a.n_bags * CS + warps - 1) / warps;
   const uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
   const unsigned grid = static_cast<unsigned>(need < cap ? need : cap);
   cudaLaunchConfig_t cfg = {};
@@ -427,36 +453,36 @@ static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   return check_launch("k_bag");
 }
 
-template <int R, int NPL, bool TAB, uint32_t GW, bool BF16>
+template <int R, int NPL, bool TAB, uint32_t GW, bool BF16, int CS = 1>
 static int launch_bag_sc(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   switch (plan->S) {
-    case 1: return launch_bag_t<R, 1, NPL, TAB, GW, BF16>(plan, a, stream);
-    case 2: return launch_bag_t<R, 2, NPL, TAB, GW, BF16>(plan, a, stream);
-    case 4: return launch_bag_t<R, 4, NPL, TAB, GW, BF16>(plan, a, stream);
-    case 8: return launch_bag_t<R, 8, NPL, TAB, GW, BF16>(plan, a, stream);
-    default: return launch_bag_t<R, 16, NPL, TAB, GW, BF16>(plan, a, stream);
+    case 1: return launch_bag_t<R, 1, NPL, TAB, GW, BF16, (CS <= 1 ? CS : 1)>(plan, a, stream);
+    case 2: return launch_bag_t<R, 2, NPL, TAB, GW, BF16, (CS <= 2 ? CS : 1)>(plan, a, stream);
+    case 4: return launch_bag_t<R, 4, NPL, TAB, GW, BF16, (CS <= 4 ? CS : 1)>(plan, a, stream);
+    case 8: return launch_bag_t<R, 8, NPL, TAB, GW, BF16, (CS <= 8 ? CS : 1)>(plan, a, stream);
+    default: return launch_bag_t<R, 16, NPL, TAB, GW, BF16, (CS <= 16 ? CS : 1)>(plan, a, stream);
   }
 }
 
-template <int R, uint32_t GW, bool BF16>
+template <int R, uint32_t GW, bool BF16, int CS = 1>
 static int launch_bag_table(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   switch (plan->view.npl) {
-    case 0: return launch_bag_sc<R, 0, true, GW, BF16>(plan, a, stream);
-    case 1: return launch_bag_sc<R, 1, true, GW, BF16>(plan, a, stream);
-    default: return launch_bag_sc<R, 6, true, GW, BF16>(plan, a, stream);
+    case 0: return launch_bag_sc<R, 0, true, GW, BF16, CS>(plan, a, stream);
+    case 1: return launch_bag_sc<R, 1, true, GW, BF16, CS>(plan, a, stream);
+    default: return launch_bag_sc<R, 6, true, GW, BF16, CS>(plan, a, stream);
   }
 }
 
-template <uint32_t GW, bool BF16>
+template <uint32_t GW, bool BF16, int CS = 1>
 static int launch_bag_gw(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   if (!plan->uniform)
-    return plan->max_runs <= 2 ? launch_bag_table<2, GW, BF16>(plan, a, stream)
-                               : launch_bag_table<4, GW, BF16>(plan, a, stream);
+    return plan->max_runs <= 2 ? launch_bag_table<2, GW, BF16, CS>(plan, a, stream)
+                               : launch_bag_table<4, GW, BF16, CS>(plan, a, stream);
   switch (plan->max_runs) {
-    case 1: return launch_bag_sc<1, 0, false, GW, BF16>(plan, a, stream);
-    case 2: return launch_bag_sc<2, 0, false, GW, BF16>(plan, a, stream);
-    case 3: return launch_bag_sc<3, 0, false, GW, BF16>(plan, a, stream);
-    default: return launch_bag_sc<4, 0, false, GW, BF16>(plan, a, stream);
+    case 1: return launch_bag_sc<1, 0, false, GW, BF16, CS>(plan, a, stream);
+    case 2: return launch_bag_sc<2, 0, false, GW, BF16, CS>(plan, a, stream);
+    case 3: return launch_bag_sc<3, 0, false, GW, BF16, CS>(plan, a, stream);
+    default: return launch_bag_sc<4, 0, false, GW, BF16, CS>(plan, a, stream);
   }
 }
 
@@ -465,5 +491,7 @@ int launch_bag_256(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
 int launch_bag_512(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
 int launch_bag_1024(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);
 int launch_bag_bf16(const ibp_plan* plan, BagArgs& a, cudaStream_t stream);  // 512-word groups
+// 1024-word groups, teams of 2 or 4 warps per bag (device slots, few bags)
+int launch_bag_1024_split(const ibp_plan* plan, BagArgs& a, cudaStream_t stream, int cs);
 
 }  // namespace ibp

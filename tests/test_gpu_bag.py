@@ -205,3 +205,24 @@ def test_bag_bf16_rows_match_oracle(W, where):
         st, dec = C.decompress(words_np(g["slots_t"]), g["bitmask"], ids, g["mask"], g["bitval"])
         _, want = B.embedding_bag(dec, offsets, mode, bf16=True)
         assert np.array_equal(out.cpu().numpy().view(np.uint32), want)
+
+
+@pytest.mark.parametrize("W", [128, 256, 512])
+@pytest.mark.parametrize("n_bags", [40, 300, 900])
+def test_few_large_bags_from_hbm(W, n_bags):
+    """Few bags on device slots are pooled by teams of warps that split the
+    segments; each column is still added in bag order."""
+    rng = np.random.default_rng(500 + W + n_bags)
+    n = max(200, 150_000 // W)
+    per_column = W == 256
+    rows = _rows(rng, n, W, per_column=per_column)
+    g = gpu_codec(rows, np.delete(rows, np.s_[::9], axis=0), 0.95 if per_column else 0.9, "hbm")
+    sizes = rng.integers(0, 60, n_bags)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    ids = rng.integers(0, n, int(offsets[-1])).astype(np.int64)
+    for mode in (ibp.IBP_BAG_SUM, ibp.IBP_BAG_MEAN):
+        out = ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]),
+                                            torch.from_numpy(ids).cuda(), torch.from_numpy(offsets).cuda(), mode)
+        assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
+        st, want = _expected(g, ids, offsets, mode)
+        assert st == 0 and np.array_equal(out.cpu().numpy().view(np.uint32), want)
