@@ -178,11 +178,11 @@ def kernel_sources_sha() -> str:
     return h.hexdigest()
 
 
-def kernel_traffic(kind: str) -> dict:
+def kernel_traffic(kind: str, config: str) -> dict:
     """Measured traffic per launch of one bench leg from the committed ncu
-    summary, when it was taken on the current kernel sources (else {}):
-    dram = DRAM bytes read + written; link = bytes over the host link
-    (sysmem sectors x 32)."""
+    summary, when it was taken on this workload and the current kernel sources
+    (else {}): dram = DRAM bytes read + written; link = bytes over the host
+    link (sysmem sectors x 32)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         rec = json.load(open(path))
@@ -190,7 +190,7 @@ def kernel_traffic(kind: str) -> dict:
     except (OSError, ValueError):
         return {}
     ent = rec.get(kind)
-    if not ent or ent.get("kernel_source_sha256") != sha:
+    if not ent or ent.get("kernel_source_sha256") != sha or ent.get("config") != config:
         return {}
     return {"dram": ent.get("dram_bytes_read", 0) + ent.get("dram_bytes_write", 0),
             "link": ent.get("link_bytes")}
@@ -587,9 +587,9 @@ def run_ours(args):
     host_achieved = link_bytes_launch / (launch_ms * 1e-3) / 1e9
     hbm_alg_bytes = (link_words * 4 + K * B * (4 * W + 8) + K * B / 8) / K
     hbm_achieved = hbm_alg_bytes / (hbm_launch_ms * 1e-3) / 1e9
-    traffic_host = kernel_traffic("host_resident")
-    traffic_hbm = kernel_traffic("hbm_resident")
-    traffic_pk = kernel_traffic("packed_hbm_cache")
+    traffic_host = kernel_traffic("host_resident", name)
+    traffic_hbm = kernel_traffic("hbm_resident", name)
+    traffic_pk = kernel_traffic("packed_hbm_cache", name)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
