@@ -189,8 +189,8 @@ def kernel_traffic(kind: str, config: str) -> dict:
         sha = kernel_sources_sha()
     except (OSError, ValueError):
         return {}
-    ent = rec.get(kind)
-    if not ent or ent.get("kernel_source_sha256") != sha or ent.get("config") != config:
+    ent = rec.get(config, {}).get(kind)
+    if not ent or ent.get("kernel_source_sha256") != sha:
         return {}
     return {"dram": ent.get("dram_bytes_read", 0) + ent.get("dram_bytes_write", 0),
             "link": ent.get("link_bytes")}
