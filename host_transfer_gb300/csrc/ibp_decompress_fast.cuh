@@ -468,6 +468,11 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   int occ = occ_cache[dev];
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    // Row-reuse copies are served from L1: prefer a quarter of the SM's
+    // on-chip memory as shared memory and leave the rest to L1 (DLRM rows,
+    // Zipf ids: 279 -> 286 GB/s; a smaller share left too few CTAs).
+    if (GW == kGroupWordsReuse && e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 25);
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, static_cast<int>(warps * 32), smem);
     if (e != cudaSuccess || occ < 1) {
