@@ -224,9 +224,63 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     }
   };
 
+  // Bits that the matching words of a row save against 32 bits each (p per
+  // match, plus pscale * e for the e-planes of per-word plans), summed over
+  // its S headers.  Rows of 8 or more segments: one header per lane, G rows
+  // in ceil(G / (32 / SC)) passes, each row's sum by a warp reduction and
+  // kept by lane q for row q (warp-collective: every lane calls it).
+  // Shorter rows: lane q walks its own row's headers.
+  auto saved_bits = [&](const uint32_t* sb) -> uint32_t {
+    auto seg_saved = [&](uint32_t H, uint32_t s) -> uint32_t {
+      uint32_t c = p * __popc(H);
+      if constexpr (TAB && NPL > 0) {
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) c += pscale * (__popc(H & epl[s * NPL + k]) << k);
+      }
+      return c;
+    };
+    uint32_t mine = 0;
+    if constexpr (SC >= 8) {
+      constexpr uint32_t RPP = SC >= 32 ? 1u : 32u / SC;  // rows per pass
+      const uint32_t qo = SC >= 32 ? 0u : lane / SC;       // this lane's row in a pass
+#pragma unroll
+      for (uint32_t q0 = 0; q0 < G; q0 += RPP) {
+        uint32_t c = 0;
+        if (q0 + qo < G) {
+          const uint32_t* hb = sb + (q0 + qo) * W;
+#pragma unroll
+          for (uint32_t s = SC >= 32 ? lane : lane % SC; s < SC; s += 32) c += seg_saved(hb[s], s);
+        }
+#pragma unroll
+        for (uint32_t r = 0; r < RPP; ++r) {
+          if (q0 + r >= G) break;
+          const uint32_t t = __reduce_add_sync(kAll, qo == r ? c : 0u);
+          if (lane == q0 + r) mine = t;
+        }
+      }
+    } else {
+      if (lane < G) {
+        const uint32_t* hb = sb + lane * W;
+        if constexpr (SC >= 4) {
+#pragma unroll
+          for (uint32_t s = 0; s < SC; s += 4) {
+            const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
+            mine += seg_saved(h.x, s) + seg_saved(h.y, s + 1) + seg_saved(h.z, s + 2) + seg_saved(h.w, s + 3);
+          }
+        } else {
+#pragma unroll
+          for (uint32_t s = 0; s < SC; ++s) mine += seg_saved(hb[s], s);
+        }
+      }
+    }
+    return mine;
+  };
+
   // Kind and stream length of lane q's row of group j (headers in stage).
+  // Warp-collective (saved_bits).
   auto row_info = [&](const uint32_t* sb, int32_t id, RowPos rp, uint32_t bmw, uint32_t& kind,
                       uint32_t& nt) {
+    const uint32_t saved = saved_bits(sb);
     kind = kNone;
     nt = 0;
     if (id == kNoRow) return;
@@ -243,30 +297,7 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
       kind = kCorrupt;
       return;
     }
-    const uint32_t* hb = sb + lane * W;
-    uint32_t m = 0;  // matching words
-    uint32_t me = 0;  // sum of e over the matching words (TAB)
-    auto count = [&](uint32_t H, uint32_t s) {
-      m += __popc(H);
-      if constexpr (TAB && NPL > 0) {
-#pragma unroll
-        for (int k = 0; k < NPL; ++k) me += __popc(H & epl[s * NPL + k]) << k;
-      }
-    };
-    if constexpr (SC >= 4) {
-#pragma unroll
-      for (uint32_t s = 0; s < SC; s += 4) {
-        const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
-        count(h.x, s);
-        count(h.y, s + 1);
-        count(h.z, s + 2);
-        count(h.w, s + 3);
-      }
-    } else {
-#pragma unroll
-      for (uint32_t s = 0; s < SC; ++s) count(hb[s], s);
-    }
-    const uint32_t Lw = (32u * (SC + W) - p * m - pscale * me + 31u) >> 5;
+    const uint32_t Lw = (32u * (SC + W) - saved + 31u) >> 5;
     if (Lw >= W || (PK && ((Lw + 3u) & ~3u) > rp.ext)) {
       kind = kCorrupt;
       return;
