@@ -157,7 +157,59 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
     }
   };
 
+  // Bits saved by the matching words of lane q's row (summed over its
+  // headers), as in k_decompress_fast: rows of 8 or more segments take one
+  // header per lane and a warp reduction per row (warp-collective), shorter
+  // rows a walk by lane q.
+  auto saved_bits = [&](const uint32_t* sb) -> uint32_t {
+    auto seg_saved = [&](uint32_t H, uint32_t s) -> uint32_t {
+      uint32_t c = p * __popc(H);
+      if constexpr (TAB && NPL > 0) {
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) c += pscale * (__popc(H & epl[s * NPL + k]) << k);
+      }
+      return c;
+    };
+    uint32_t mine = 0;
+    if constexpr (SC >= 8) {
+      constexpr uint32_t RPP = SC >= 32 ? 1u : 32u / SC;  // rows per pass
+      const uint32_t qo = SC >= 32 ? 0u : lane / SC;
+#pragma unroll
+      for (uint32_t q0 = 0; q0 < G; q0 += RPP) {
+        uint32_t c = 0;
+        if (q0 + qo < G) {
+          const uint32_t* hb = sb + (q0 + qo) * W;
+#pragma unroll
+          for (uint32_t s = SC >= 32 ? lane : lane % SC; s < SC; s += 32) c += seg_saved(hb[s], s);
+        }
+#pragma unroll
+        for (uint32_t r = 0; r < RPP; ++r) {
+          if (q0 + r >= G) break;
+          const uint32_t t = __reduce_add_sync(kAll, qo == r ? c : 0u);
+          if (lane == q0 + r) mine = t;
+        }
+      }
+    } else {
+      if (lane < G) {
+        const uint32_t* hb = sb + lane * W;
+        if constexpr (SC >= 4) {
+#pragma unroll
+          for (uint32_t s = 0; s < SC; s += 4) {
+            const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
+            mine += seg_saved(h.x, s) + seg_saved(h.y, s + 1) + seg_saved(h.z, s + 2) + seg_saved(h.w, s + 3);
+          }
+        } else {
+#pragma unroll
+          for (uint32_t s = 0; s < SC; ++s) mine += seg_saved(hb[s], s);
+        }
+      }
+    }
+    return mine;
+  };
+
+  // Warp-collective (saved_bits).
   auto row_info = [&](const uint32_t* sb, int32_t id, uint32_t bmw, uint32_t& kind, uint32_t& nt) {
+    const uint32_t saved = saved_bits(sb);
     kind = kNone;
     nt = 0;
     if (id == kNoRow) return;
@@ -170,29 +222,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
       nt = W;
       return;
     }
-    const uint32_t* hb = sb + lane * W;
-    uint32_t m = 0, me = 0;
-    auto count = [&](uint32_t H, uint32_t s) {
-      m += __popc(H);
-      if constexpr (TAB && NPL > 0) {
-#pragma unroll
-        for (int k = 0; k < NPL; ++k) me += __popc(H & epl[s * NPL + k]) << k;
-      }
-    };
-    if constexpr (SC >= 4) {
-#pragma unroll
-      for (uint32_t s = 0; s < SC; s += 4) {
-        const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
-        count(h.x, s);
-        count(h.y, s + 1);
-        count(h.z, s + 2);
-        count(h.w, s + 3);
-      }
-    } else {
-#pragma unroll
-      for (uint32_t s = 0; s < SC; ++s) count(hb[s], s);
-    }
-    const uint32_t Lw = (32u * (SC + W) - p * m - pscale * me + 31u) >> 5;
+    const uint32_t Lw = (32u * (SC + W) - saved + 31u) >> 5;
     if (Lw >= W) {
       kind = kCorrupt;
       return;
