@@ -49,3 +49,22 @@ def test_two_rank_replicas_gloo():
     assert all(r[3] == 2.0 for r in res)  # max over ranks
     a, b = res[0][4], res[1][4]
     assert a.shape == b.shape and not np.array_equal(a, b)
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """Two ranks launched as the multi-GPU bench is: rank 0 alone times the
+    oracle and prints the line; the other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--rows", "20000", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
