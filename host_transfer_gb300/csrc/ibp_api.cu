@@ -19,6 +19,8 @@ void set_cuda_error(cudaError_t e, const char* where) {
   snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
 }
 
+void set_detail(const char* text) { snprintf(g_detail, sizeof(g_detail), "%s", text); }
+
 void clear_error_detail() { g_detail[0] = 0; }
 
 int check_launch(const char* where) {
@@ -495,6 +497,8 @@ int ibp_get_status(const ibp_plan* plan, void* stream) {
   if (!plan) return IBP_EINVAL;
   DeviceGuard g(plan->device);
   if (!g.ok) return IBP_ECUDA;
+  // h_status is the plan's one pinned word: one caller at a time
+  std::lock_guard<std::mutex> lock(const_cast<ibp_plan*>(plan)->status_mu);
   // one copy into the plan's pinned word, ordered on the stream, then one wait
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(plan->h_status, plan->view.status, 4, cudaMemcpyDeviceToHost, s);
@@ -510,6 +514,29 @@ int ibp_get_status(const ibp_plan* plan, void* stream) {
     return IBP_ECUDA;
   }
   return static_cast<int>(st);
+}
+
+}  // extern "C"
+
+// Moves the status word to *dst and clears it, in one atomic exchange (so an
+// error recorded concurrently by another stream's kernel is either moved or
+// kept, never lost).
+__global__ void k_take_status(uint32_t* status, uint32_t* dst) {
+  if (threadIdx.x == 0) *dst = atomicExch(status, 0u);
+}
+
+extern "C" {
+
+int ibp_get_status_async(const ibp_plan* plan, uint32_t* status_out, void* stream) {
+  g_detail[0] = 0;
+  if (!plan || !status_out) return IBP_EINVAL;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return IBP_ECUDA;
+  const void* dst;
+  if (resolve_ptr(status_out, plan->device, &dst)) return IBP_EINVAL;
+  k_take_status<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      plan->view.status, const_cast<uint32_t*>(static_cast<const uint32_t*>(dst)));
+  return check_launch("k_take_status");
 }
 
 int ibp_row_lengths(const ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "ibp.h"
 
 namespace ibp {
@@ -73,6 +75,7 @@ struct ibp_plan {
   uint32_t prefix;  // words fetched before the headers (slot layout); 0 = from lmin
   void* d_block;  // single device allocation holding every table + status
   uint32_t* h_status;  // pinned host word the status is read back into
+  std::mutex status_mu;  // serialises ibp_get_status calls on this plan (h_status)
   size_t d_bytes;
   ibp::PlanView view;
 };
@@ -83,6 +86,8 @@ namespace ibp {
 // Host-side helpers (ibp_api.cu)
 
 void set_cuda_error(cudaError_t e, const char* where);
+// Plain text for ibp_last_error_detail (argument errors, not CUDA errors).
+void set_detail(const char* text);
 void clear_error_detail();
 int check_launch(const char* where);
 // Resolves a pointer to an address a kernel on `device` can dereference.

@@ -9,6 +9,7 @@
 // its counters live in the file-scope array below, a fixed
 // IBP_NOALLOC_MAX_W * 32 words (512 KiB) that every GPU which loads the library
 // keeps until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -21,17 +22,52 @@ namespace ibp {
 // call on a device; each call clears the part it uses before counting.
 static __device__ __align__(256) uint32_t g_noalloc_ones[IBP_NOALLOC_MAX_W * 32];
 
-// Device address of g_noalloc_ones, looked up once per device.  In host code
-// the name g_noalloc_ones is only a host-side stand-in for the symbol, never a
-// device address, so kernels always get the looked-up pointer.
+// Device address of g_noalloc_ones per device, with the id of the context it
+// was looked up in.  In host code the name g_noalloc_ones is only a host-side
+// stand-in for the symbol, never a device address, so kernels always get the
+// looked-up pointer.  The module (and so the array) is loaded anew in a new
+// context, e.g. after cudaDeviceReset, and may then sit at another address:
+// the context id tells a stale entry from a valid one.
 static std::mutex g_noalloc_mu;
-static uint32_t* g_noalloc_ptr[64] = {nullptr};
+struct NoallocEntry {
+  unsigned long long ctx_id;
+  uint32_t* ptr;
+};
+static NoallocEntry g_noalloc[64] = {};
 
+// cuCtxGetId of the current context, through the runtime's driver entry
+// point (the library does not link the driver library itself).
+static int current_ctx_id(unsigned long long* id) {
+  using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+  static CtxGetId fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f) {
+      set_cuda_error(e != cudaSuccess ? e : cudaErrorSymbolNotFound, "cudaGetDriverEntryPointByVersion(cuCtxGetId)");
+      cudaGetLastError();
+      return IBP_ECUDA;
+    }
+    fn = reinterpret_cast<CtxGetId>(f);
+  }
+  if (fn(nullptr, id) != CUDA_SUCCESS) {
+    set_detail("cuCtxGetId: no current context");
+    return IBP_ECUDA;
+  }
+  return IBP_OK;
+}
+
+// `device` is the current device.  Looks the array up the first time it is
+// used in the device's current context.
 static int noalloc_scratch(int device, uint32_t** out) {
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (device < 0 || device >= 64) return IBP_EINVAL;
-  if (!g_noalloc_ptr[device]) {
-    // `device` is current here (the caller's current device).
+  unsigned long long ctx = 0;
+  int rc = current_ctx_id(&ctx);
+  if (rc != IBP_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocEntry& ent = g_noalloc[device];
+  if (!ent.ptr || ent.ctx_id != ctx) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_ones);
     if (e != cudaSuccess || p == nullptr) {
@@ -39,9 +75,10 @@ static int noalloc_scratch(int device, uint32_t** out) {
       cudaGetLastError();
       return IBP_ECUDA;
     }
-    g_noalloc_ptr[device] = static_cast<uint32_t*>(p);
+    ent.ptr = static_cast<uint32_t*>(p);
+    ent.ctx_id = ctx;
   }
-  *out = g_noalloc_ptr[device];
+  *out = ent.ptr;
   return IBP_OK;
 }
 
@@ -53,7 +90,7 @@ extern "C" int ibp_preprocess_noalloc(const uint32_t* sample, uint64_t s_rows, u
                                       uint32_t* mask, uint32_t* bitval, void* stream) {
   clear_error_detail();
   if (W > IBP_NOALLOC_MAX_W) {
-    set_cuda_error(cudaErrorInvalidValue, "ibp_preprocess_noalloc: W is above IBP_NOALLOC_MAX_W (4096)");
+    set_detail("ibp_preprocess_noalloc: W is above IBP_NOALLOC_MAX_W (4096)");
     return IBP_EINVAL;
   }
   if (W == 0 || s_rows == 0 || s_rows >= (1ull << 32)) return IBP_EINVAL;

@@ -90,6 +90,7 @@ def load():
         "ibp_gather_decompress": ([vp, vp, u64, vp, vp, u64, vp, vp], i32),
         "ibp_decompress_contig": ([vp, vp, u64, vp, u64, u64, vp, vp], i32),
         "ibp_get_status": ([vp, vp], i32),
+        "ibp_get_status_async": ([vp, vp, vp], i32),
         "ibp_gather_raw": ([vp, u64, u32, vp, u64, vp, vp], i32),
         "ibp_row_lengths": ([vp, vp, u64, vp, vp, u64, vp, vp], i32),
         "ibp_packed_offsets": ([vp, vp, u64, vp, vp, vp], i32),
@@ -319,6 +320,18 @@ def ibp_get_status(plan: Plan, stream=None, raise_on_error: bool = True) -> int:
     if raise_on_error and code != IBP_OK:
         raise IbpError(code, "ibp_get_status")
     return code
+
+
+def ibp_get_status_async(plan: Plan, status_out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Enqueue the move of the plan's status word into `status_out` (one int32
+    word of pinned host or device memory; a view of a larger tensor is fine)
+    and return without waiting: read it after synchronising with the stream."""
+    lib = load()
+    if status_out.element_size() != 4 or not status_out.is_contiguous():
+        raise ValueError("status_out must be a contiguous 32-bit word")
+    _check(lib.ibp_get_status_async(plan.handle, _ptr(status_out), _stream(stream, plan.device)),
+           "ibp_get_status_async")
+    return status_out
 
 
 def ibp_row_lengths(plan: Plan, slots: torch.Tensor, bitmask: torch.Tensor, row_ids: torch.Tensor,

@@ -146,10 +146,13 @@ int ibp_preprocess(const uint32_t* sample, uint64_t s_rows, uint32_t W, double T
  * cudaMalloc, cudaFree or other allocating call is made.
  *
  * - W must be at most IBP_NOALLOC_MAX_W; a larger W returns IBP_EINVAL before
- *   anything runs.
+ *   anything runs, and ibp_last_error_detail() then names the limit.
  * - The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
- *   capture.
+ *   capture.  The address is kept with the id of the device's context: after
+ *   cudaDeviceReset, or any other new context on the device, the module is
+ *   loaded again and the next call looks the address up again (that call,
+ *   too, belongs before any capture).
  * - Every call on a device shares the one array, and each call clears the part
  *   it uses on `stream` before counting: calls that overlap on the GPU (on
  *   different streams, without ordering between them) race and give wrong
@@ -406,9 +409,27 @@ int ibp_plan_set_get_status(const ibp_plan_set* set, void* stream);
 /*
  * Synchronises `stream`, returns the first data error recorded by the plan's
  * kernels since the last call (IBP_OK if none) and clears it.  The status
- * word is shared by every call made with this plan, on any stream.
+ * word is shared by every call made with this plan, on any stream.  Calls on
+ * one plan from several host threads are serialised inside the library.
  */
 int ibp_get_status(const ibp_plan* plan, void* stream);
+
+/*
+ * Status read that does not wait: enqueues on `stream` one small kernel that
+ * moves the plan's status word into *status_out and clears it (one atomic
+ * exchange), and returns at once.  Once the stream has passed that kernel,
+ * *status_out holds the first data error recorded by the plan's kernels
+ * ordered before it (IBP_OK if none); read it after synchronising with the
+ * stream (an event, cudaStreamSynchronize).  A caller can so check the result
+ * of every decompress call without stopping the GPU between calls, e.g. one
+ * word of a pinned ring per call, checked a few calls later.
+ *
+ * status_out  device-accessible uint32 (mapped pinned host memory, or device
+ *             memory), owned by the caller; written by the kernel.
+ * Errors: IBP_EINVAL (NULL plan or word, word not device-accessible),
+ * IBP_ECUDA.
+ */
+int ibp_get_status_async(const ibp_plan* plan, uint32_t* status_out, void* stream);
 
 /*
  * Fetched length per row - « Intégration au système »: a fixed-size buffer of

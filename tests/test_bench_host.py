@@ -13,20 +13,49 @@ import bench
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_reference_arm_line():
+def _reference_line(argv):
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
-        bench.main(["--impl", "reference", "--rows", "20000", "--steps", "2", "--warmup", "3"])
+        bench.main(["--impl", "reference", *argv])
     lines = [ln for ln in buf.getvalue().splitlines() if ln.startswith("{")]
     assert len(lines) == 1
-    d = json.loads(lines[0])
+    return json.loads(lines[0])
+
+
+def _check_reference(d, steps, warmup):
     assert d["impl"] == "reference"
     assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
-    assert d["steps"] == 2 and d["warmup"] == 3 and d["value"] > 0
+    assert d["steps"] == steps and d["warmup"] == warmup and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    assert "workload" in d["config"]
+
+
+def test_reference_arm_line():
+    d = _reference_line(["--config", "dense_gnn", "--rows", "20000", "--steps", "2", "--warmup", "3"])
+    _check_reference(d, 2, 3)
+    args = bench.parse_args(["--config", "dense_gnn", "--rows", "20000"])
+    assert d["config"] == bench.config_of("dense_gnn", args, 1)  # the GPU arm prints the same object
+    assert "65,536 ids" in d["cpu_baseline"]["sample"]  # a whole batch per step, as on the GPU
+
+
+def test_reference_arm_llm_decodes_whole_layers():
+    """The default config's reference arm: the headline (LLM offload) with
+    whole layers per step, as the GPU arm decodes them."""
+    d = _reference_line(["--layers", "2", "--steps", "1", "--warmup", "3"])
+    _check_reference(d, 1, 3)
+    args = bench.parse_args(["--layers", "2"])
+    assert d["config"] == bench.config_of("llm", args, 1)
+    assert "whole layer" in d["cpu_baseline"]["sample"]
+
+
+def test_output_ring_exceeds_l2():
+    class C:
+        l2 = 126 * 2**20
+
+    for out_bytes in (33_554_432, 67_108_864, 100_663_296, 300_000_000):
+        n = bench.Ctx.ring_count(C(), out_bytes)
+        assert n >= 2 and n * out_bytes >= 2 * C.l2
 
 
 def test_reference_arm_rejects_short_warmup():

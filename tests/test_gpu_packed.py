@@ -8,6 +8,7 @@ import torch
 
 from host_transfer_gb300 import ibp, workloads
 from oracle import oracle_c as C
+from oracle import packed_ref as P
 from tests.gpu_util import gpu_codec, on_device, pinned, words_np
 
 pytestmark = pytest.mark.gpu
@@ -23,13 +24,9 @@ def _lib():
 
 
 def _expected(rows, mask, bitval):
-    """Offsets and packed words from the oracle: row r keeps the first
-    round_up(stored words, 4) words of its slot."""
+    """Offsets and packed words of the oracle's slots (oracle/packed_ref.py)."""
     slots, bitmask, _ = C.compress(rows, mask, bitval)
-    words = C.row_words(rows, mask, bitval).astype(np.int64)
-    lens = (words + 3) // 4 * 4
-    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
-    packed = np.concatenate([slots[r, :lens[r]] for r in range(len(rows))]) if len(rows) else np.zeros(0, np.uint32)
+    offsets, packed = P.pack(slots, C.row_words(rows, mask, bitval))
     return offsets, packed, bitmask
 
 

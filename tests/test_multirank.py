@@ -61,7 +61,7 @@ def test_reference_arm_under_torchrun_prints_one_line():
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
-           "--impl", "reference", "--gpus", "2", "--rows", "20000", "--steps", "1", "--warmup", "3"]
+           "--impl", "reference", "--gpus", "2", "--config", "dense_gnn", "--rows", "20000", "--steps", "1", "--warmup", "3"]
     r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]

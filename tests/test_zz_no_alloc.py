@@ -1,5 +1,5 @@
 """ibp_preprocess_noalloc - the preprocess entry point that allocates nothing -
-checked through the C ABI against ibp_preprocess.
+checked through the C ABI against ibp_preprocess and against the oracle.
 
 Some callers cannot let a library allocate device memory: a process whose
 device memory is all owned by its own allocator, or a device without
@@ -17,10 +17,13 @@ import pytest
 import torch
 
 from host_transfer_gb300 import ibp
+from oracle import oracle_c as C
 
 pytestmark = pytest.mark.gpu
 
 IBP_NOALLOC_MAX_W = 4096
+# CUmemPool_attribute values (cuda.h): the used-memory high watermark of a pool
+CU_MEMPOOL_ATTR_USED_MEM_HIGH = 8
 
 
 def _call(lib, name, sample, T, mask, bitval):
@@ -36,7 +39,28 @@ def _sample(seed, n, W):
     return torch.from_numpy(x).cuda()
 
 
-def test_noalloc_matches_preprocess_on_calls_in_a_row():
+class _DefaultPool:
+    """The high watermark of the current device's default stream-ordered memory
+    pool (where cudaMallocAsync takes its memory), read through the driver."""
+
+    def __init__(self):
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        dev = ctypes.c_int()
+        assert self.cu.cuDeviceGet(ctypes.byref(dev), torch.cuda.current_device()) == 0
+        self.pool = ctypes.c_void_p()
+        assert self.cu.cuDeviceGetDefaultMemPool(ctypes.byref(self.pool), dev) == 0
+
+    def reset_high(self):
+        zero = ctypes.c_uint64(0)  # setting 0 resets the watermark to the current use
+        assert self.cu.cuMemPoolSetAttribute(self.pool, CU_MEMPOOL_ATTR_USED_MEM_HIGH, ctypes.byref(zero)) == 0
+
+    def high(self) -> int:
+        v = ctypes.c_uint64(0)
+        assert self.cu.cuMemPoolGetAttribute(self.pool, CU_MEMPOOL_ATTR_USED_MEM_HIGH, ctypes.byref(v)) == 0
+        return v.value
+
+
+def test_noalloc_matches_preprocess_and_oracle_on_calls_in_a_row():
     from host_transfer_gb300 import build
 
     build.build()
@@ -54,6 +78,35 @@ def test_noalloc_matches_preprocess_on_calls_in_a_row():
         torch.cuda.synchronize()
         # integer results: bit-exact, the same bar as every other parity test
         assert torch.equal(m0, m1) and torch.equal(b0, b1)
+        st, m, b = C.preprocess(sample.cpu().numpy().view(np.uint32), T)
+        assert st == 0
+        assert np.array_equal(m1.cpu().numpy().view(np.uint32), m), "Mask differs from the oracle"
+        assert np.array_equal(b1.cpu().numpy().view(np.uint32), b), "Bitval differs from the oracle"
+
+
+def test_noalloc_takes_no_memory_from_the_pool():
+    """ibp_preprocess takes its scratch from the default memory pool (its call
+    raises the pool's high watermark); ibp_preprocess_noalloc must not."""
+    lib = ibp.load()
+    pool = _DefaultPool()
+    sample = _sample(5, 2048, 1024)
+    m = torch.empty(1024, dtype=torch.int32, device="cuda")
+    b = torch.empty_like(m)
+    torch.cuda.synchronize()
+    pool.reset_high()
+    before = pool.high()
+    assert _call(lib, "ibp_preprocess", sample, 0.99, m, b) == ibp.IBP_OK
+    torch.cuda.synchronize()
+    assert pool.high() >= before + 128 * 1024, "the pool check does not see a stream-ordered allocation"
+    torch.cuda.synchronize()
+    pool.reset_high()
+    before = pool.high()
+    alloc_before = torch.cuda.memory_allocated()
+    for _ in range(2):
+        assert _call(lib, "ibp_preprocess_noalloc", sample, 0.99, m, b) == ibp.IBP_OK
+    torch.cuda.synchronize()
+    assert pool.high() == before
+    assert torch.cuda.memory_allocated() == alloc_before
 
 
 def test_noalloc_rejects_rows_above_its_limit():
