@@ -36,6 +36,7 @@ One JSON line on stdout.  Every config reports:
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -543,6 +544,22 @@ class Ctx:
         del g
         return ms, clocks
 
+    def time_eager(self, step):
+        """Wall time of the K timed steps s = W .. W+K-1 issued eagerly, with one
+        synchronisation at the end; returns (seconds, seconds until the last
+        step was enqueued).  Garbage is collected first, so that no object
+        whose release synchronises the device (a plan's memory) is freed
+        inside the timed loop."""
+        gc.collect()
+        self.sync()
+        barrier(self.world)
+        t0 = time.perf_counter()
+        for s in range(self.WU, self.WU + self.K):
+            step(s)
+        t1 = time.perf_counter()
+        self.sync()
+        return time.perf_counter() - t0, t1 - t0
+
     def ring_count(self, out_bytes: int) -> int:
         """Output buffers in a ring whose total is at least twice L2, so that
         every step's writes reach DRAM rather than staying in L2."""
@@ -649,6 +666,28 @@ def run_table(ctx: Ctx, name: str, cpu_seconds: float) -> dict:
     parity = bool(np.array_equal(out_of(last).cpu().numpy().view(np.uint32), expect_last))
     launch_ms = total_ms / K
 
+    # ---- end to end through the public API ----------------------------------
+    # Eager calls as a user makes them: every step copies its ids from pinned
+    # host memory, decodes from the pinned host table, and moves its status
+    # word into pinned host memory; the host checks every step's word after
+    # the last step, so it never stalls the GPU between steps.  Run right after
+    # the graph-timed leg, over the same steps, so that both see the host
+    # table in the same state (the GPU's translations of its pages warm).
+    ids_host = torch.from_numpy(batches).pin_memory()
+    ids_step = torch.empty(B, dtype=torch.int64, device=dev)
+    status_host = torch.full((WU + K,), -1, dtype=torch.int32, pin_memory=True)
+
+    def e2e_step(s):
+        ids_step.copy_(ids_host[s % pool], non_blocking=True)      # H2D: this step's ids
+        ibp.ibp_gather_decompress(plan, table, bitmask, ids_step, out=out_of(s))
+        ibp.ibp_get_status_async(plan, status_host[s])              # D2H: this step's status
+
+    for s in range(WU):
+        e2e_step(s)
+    e2e_s, enqueue_s = ctx.time_eager(e2e_step)
+    e2e_ok = bool((status_host == 0).all().item())
+    parity = parity and e2e_ok and bool(np.array_equal(out_of(last).cpu().numpy().view(np.uint32), expect_last))
+
     # ---- HBM-resident gather-decompress ------------------------------------
     hbm_ms = ctx.time_steps(dec_hbm, f"{name}_hbm_timed") / K
     ibp.ibp_get_status(plan)
@@ -700,32 +739,6 @@ def run_table(ctx: Ctx, name: str, cpu_seconds: float) -> dict:
     pk_words = int(sum(((lens[s % pool].to(torch.int64) + 3) // 4 * 4).sum().item() for s in steps))
     pk_alg_bytes = (pk_words * 4 + K * B * (4 * W + 8 + 16) + K * B / 8) / K
     del packed, offsets
-
-    # ---- end to end through the public API ----------------------------------
-    # Eager calls as a user makes them: every step copies its ids from pinned
-    # host memory, decodes from the pinned host table, and moves its status
-    # word into pinned host memory; the host checks every step's word after
-    # the last step, so it never stalls the GPU between steps.
-    ids_host = torch.from_numpy(batches).pin_memory()
-    ids_step = torch.empty(B, dtype=torch.int64, device=dev)
-    status_host = torch.full((WU + K,), -1, dtype=torch.int32, pin_memory=True)
-
-    def e2e_step(s):
-        ids_step.copy_(ids_host[s % pool], non_blocking=True)      # H2D: this step's ids
-        ibp.ibp_gather_decompress(plan, table, bitmask, ids_step, out=out_of(s))
-        ibp.ibp_get_status_async(plan, status_host[s])              # D2H: this step's status
-
-    for s in range(WU):
-        e2e_step(s)
-    ctx.sync()
-    barrier(ctx.world)
-    t0 = time.perf_counter()
-    for s in range(WU, WU + K):
-        e2e_step(s)
-    ctx.sync()
-    e2e_s = time.perf_counter() - t0
-    e2e_ok = bool((status_host == 0).all().item())
-    parity = parity and e2e_ok and bool(np.array_equal(out_of(last).cpu().numpy().view(np.uint32), expect_last))
 
     # ---- numbers -------------------------------------------------------------
     world = ctx.world
@@ -784,7 +797,7 @@ def run_table(ctx: Ctx, name: str, cpu_seconds: float) -> dict:
         "hints": "IBP_HINT_ROW_REUSE" if hints else "none",
         "parity": "bit-exact" if parity else "MISMATCH",
         "e2e": {"value": round(e2e_gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": B * 8 + link_words * 4 // K,
-                "d2h_bytes_per_step": 4,
+                "d2h_bytes_per_step": 4, "enqueue_ms_per_step": round(1e3 * enqueue_s / K, 4),
                 "what": "eager API calls; per step the ids copied from pinned host memory, the compressed "
                         "rows read over the host link by the kernel (counted in h2d bytes) and the status word "
                         "moved into pinned host memory; wall clock, one synchronisation at the end"},
@@ -882,6 +895,27 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
         ibp.ibp_get_status(e["plan"])
     parity = check(timed_layers)
     ms = total_ms / K
+    # ---- end to end through the public API ----------------------------------
+    # Eager calls: every step decodes one layer from its pinned host slots (the
+    # kernels read the compressed bytes over the host link) and moves each
+    # tensor's status word into pinned host memory; checked after the last step.
+    # Run right after the graph-timed leg, over the same layers, so that both
+    # see the host slots in the same state (the GPU's translations of their
+    # pages warm).
+    status_host = torch.full((WU + K, 3), -1, dtype=torch.int32, pin_memory=True)
+
+    def e2e_step(s):
+        for j, e in enumerate(layers[s % L]):
+            ibp.ibp_decompress_contig(e["plan"], e["host"], e["bitmask"], 0, e["n"], out=e["out"])
+            ibp.ibp_get_status_async(e["plan"], status_host[s, j])
+
+    for s in range(WU):
+        e2e_step(s)
+    e2e_s, enqueue_s = ctx.time_eager(e2e_step)
+    e2e_ok = bool((status_host == 0).all().item())
+    parity = parity and e2e_ok and check([last % L])
+    del status_host
+
     # the launches of each kernel on their own (weight rows; K and V rows)
     w_ms = ctx.time_steps(lambda s: dec(s, ("weight",)), "llm_weight_host_timed") / K
     kv_ms = ctx.time_steps(lambda s: dec(s, ("K", "V")), "llm_kv_host_timed") / K
@@ -949,29 +983,6 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
     parity_ph = check(timed_layers)
     del ph_layers
 
-    # ---- end to end through the public API ----------------------------------
-    # Eager calls: every step decodes one layer from its pinned host slots (the
-    # kernels read the compressed bytes over the host link) and moves each
-    # tensor's status word into pinned host memory; checked after the last step.
-    status_host = torch.full((WU + K, 3), -1, dtype=torch.int32, pin_memory=True)
-
-    def e2e_step(s):
-        for j, e in enumerate(layers[s % L]):
-            ibp.ibp_decompress_contig(e["plan"], e["host"], e["bitmask"], 0, e["n"], out=e["out"])
-            ibp.ibp_get_status_async(e["plan"], status_host[s, j])
-
-    for s in range(WU):
-        e2e_step(s)
-    ctx.sync()
-    barrier(ctx.world)
-    t0 = time.perf_counter()
-    for s in steps:
-        e2e_step(s)
-    ctx.sync()
-    e2e_s = time.perf_counter() - t0
-    e2e_ok = bool((status_host == 0).all().item())
-    parity = parity and e2e_ok and check([last % L])
-
     # ---- numbers -------------------------------------------------------------
     world = ctx.world
     ms_step = max_over_ranks(ms, world)
@@ -991,10 +1002,6 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
             "link_bytes_per_launch": round(lb),
             "host_link_frac": round(lb / (kms / n_l * 1e-3) / 1e9 / ctx.h2d_gbs, 4),
             "hbm_frac": round(hbm_b / (khbm / n_l * 1e-3) / 1e9 / ctx.hbm_peak, 4)}
-    dom = max(per_kernel, key=lambda k: per_kernel[k]["host_ms_per_launch"] * per_kernel[k]["launches_per_step"])
-    pk = per_kernel[dom]
-    dom_kernel = {"weight": "k_decompress_fast (weight rows, 2048 words, host slots)",
-                  "kv": "k_decompress_fast (K/V rows, 64 words, host slots)"}[dom]
     hbm_step_bytes = link_step + step_bytes
     res = {
         "value": round(value, 3), "unit": "GB/s", "ms_per_step": round(ms_step, 4),
@@ -1005,17 +1012,20 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
         "h2d_gbs": round(ctx.h2d_gbs, 2),
         "host_ceiling_gbs": round(ctx.h2d_gbs / f, 2),
         "frac_of_host_ceiling": round(value / world / (ctx.h2d_gbs / f), 4),
-        "roofline": roofline("host_link", pk["link_bytes_per_launch"] / (pk["host_ms_per_launch"] * 1e-3) / 1e9,
-                             ctx.h2d_gbs, h2d_src, dom_kernel, pk["link_bytes_per_launch"], None,
-                             traffic_source="no ncu record for this workload",
-                             step={"achieved": round(link_step / (ms * 1e-3) / 1e9, 2),
-                                   "frac": round(link_step / (ms * 1e-3) / 1e9 / ctx.h2d_gbs, 4),
-                                   "bytes_per_step": round(link_step)}),
+        # every launch of the step is k_decompress_fast (the weight's, K's and
+        # V's instantiation): bytes per launch and launch time are the step's
+        # over its three launches; "kernels" splits them, each timed alone
+        "roofline": roofline("host_link", link_step / (ms * 1e-3) / 1e9, ctx.h2d_gbs, h2d_src,
+                             "k_decompress_fast (weight, K, V of one layer: 3 launches per step, host slots)",
+                             link_step / 3, kernel_traffic("host_resident", "llm").get("link"),
+                             traffic_source="ncu: host-link bytes (sysmem sectors x 32) per launch",
+                             bytes_per_step=round(link_step)),
         "kernels": per_kernel,
         "hbm_resident": {
             "value": round(step_bytes / (hbm_ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(hbm_ms, 4),
             "roofline": roofline("hbm", hbm_step_bytes / (hbm_ms * 1e-3) / 1e9, ctx.hbm_peak, ctx.hbm_peak_src,
-                                 "k_decompress_fast (weight, K, V of one layer; slots in HBM)", hbm_step_bytes, None,
+                                 "k_decompress_fast (weight, K, V of one layer: 3 launches per step, slots in HBM)",
+                                 hbm_step_bytes / 3, kernel_traffic("hbm_resident", "llm").get("dram"),
                                  output="each layer has its own 96 MiB of outputs (32 layers: 3 GiB > L2)")},
         "kv_per_head": {
             "what": "K and V with one Mask/Bitval per attention head (32 plans per tensor, plan-set decode); "
@@ -1028,7 +1038,7 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
             "parity": "bit-exact" if parity_ph else "MISMATCH"},
         "parity": "bit-exact" if parity else "MISMATCH",
         "e2e": {"value": round(e2e_gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": round(link_step),
-                "d2h_bytes_per_step": 12,
+                "d2h_bytes_per_step": 12, "enqueue_ms_per_step": round(1e3 * enqueue_s / K, 4),
                 "what": "eager API calls; per step one layer's compressed slots read from pinned host memory by "
                         "the kernels (the step's host-to-device bytes) and three status words moved into pinned "
                         "host memory; wall clock, one synchronisation at the end"},

@@ -13,8 +13,9 @@
 // gives zeros and IBP_ERANGE; a bad id or a corrupt slot decodes to a zero
 // row that still counts in the bag's size (IBP_ERANGE / IBP_ECORRUPT).
 //
-// The fetch and decode are those of k_decompress_fast (same plan shapes, same
-// three-stage cp.async pipeline of prefix, then rest, per group of G rows).
+// The fetch and decode steps are those of k_decompress_fast (RowPipe in
+// ibp_decode_pipe.cuh: same plan shapes, same three-stage cp.async pipeline
+// of prefix, then rest, per group of G rows).
 // What differs is the unit of work: warp gw owns bags gw, gw + nwarps, ...; a
 // cursor cuts each bag into groups of at most G consecutive ids (a group
 // never spans two bags; an empty or invalid bag is one group of no rows), and
@@ -38,52 +39,21 @@ namespace ibp {
 template <int R, int SC, int NPL, bool TAB, uint32_t GW, bool BF16, int CS = 1>
 __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   static_assert(CS >= 1 && SC % CS == 0, "a warp pools whole segments");
-  using F = FastShape<SC, GW>;
-  using T = TabShape<SC, R, NPL, TAB>;
-  constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
-  constexpr uint32_t EW = TabEntry<R>::EW;
+  using Pipe = RowPipe<R, SC, NPL, TAB, false, GW>;
+  using F = typename Pipe::F;
+  using T = typename Pipe::T;
+  constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE;
   constexpr int D = kFastStages;
   extern __shared__ __align__(128) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t nw_cta = blockDim.x >> 5;
-  uint32_t* const tab = smem;
-  uint32_t* const epl = smem + T::ENT;
   uint32_t* const stages = smem + T::WORDS + warp * static_cast<uint32_t>(D) * STAGE;
-  const uint32_t lt = lanemask_lt();
-  const uint32_t lanebit = 1u << lane;
 
   const PlanView pv = ba.d.pv;
-  const uint32_t* const slots = ba.d.slots;
-  const uint32_t* const bitmask = ba.d.bitmask;
   const int64_t* const ids = ba.d.ids;
-  const uint32_t p = TAB ? pv.p_min : pv.u_p;
-  const uint32_t pscale = pv.p_scale;
-  const uint32_t bm = pv.u_bm;
-  uint32_t rm[R], rs[R];
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-    rm[k] = pv.u_rmask[k];
-    rs[k] = pv.u_rsh[k];
-  }
-  if constexpr (TAB) {
-    for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
-      uint32_t* e = tab + w * EW;
-#pragma unroll
-      for (int k = 0; k < (EW == 4 ? 2 : 4); ++k) e[k] = k < R ? __ldg(pv.rmask + k * W + w) : 0u;
-      e[EW == 4 ? 2 : 4] = __ldg(pv.rshift + w);
-      e[EW == 4 ? 3 : 5] = __ldg(pv.bm + w);
-    }
-    if constexpr (NPL > 0) {
-      for (uint32_t i = threadIdx.x; i < SC * NPL; i += blockDim.x)
-        epl[i] = __ldg(pv.eplanes + (i / NPL) * kPlanes + (i % NPL));
-    }
-    __syncthreads();
-  }
-  const bool reuse = (pv.hints & IBP_HINT_ROW_REUSE) != 0;
-  const uint32_t pre = ba.d.pre;  // multiple of 4, <= W
-  const uint32_t pre_ch = pre >> 2;
-  const uint32_t n_rows32 = static_cast<uint32_t>(ba.d.n_rows);  // < 2^31 (checked by the launcher)
+  Pipe pp;
+  pp.init(pv, ba.d.slots, ba.d.bitmask, nullptr, ba.d.n_rows, ba.d.pre, smem);
   const uint64_t n_bags = ba.n_bags;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nw_cta + warp;
   const uint64_t nwarps = static_cast<uint64_t>(gridDim.x) * nw_cta;
@@ -133,113 +103,9 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   };
 
   // Row ids of a group: lane q < n holds the id at position pos + q.
-  constexpr int32_t kNoRow = -1, kBadId = -2;
   auto load_id = [&](const Grp& g) -> int32_t {
     if (g.bag >= n_bags || lane >= g.n) return kNoRow;
-    const int64_t id = ids[g.pos + lane];
-    return (id >= 0 && static_cast<uint64_t>(id) < n_rows32) ? static_cast<int32_t>(id) : kBadId;
-  };
-
-  auto issue_prefix = [&](uint32_t* sb, int32_t id, uint32_t& bmw) {
-    if (id >= 0) bmw = ld_u32(bitmask + (static_cast<uint32_t>(id) >> 5));
-#pragma unroll
-    for (uint32_t q = 0; q < G; ++q) {
-      const int32_t idq = __shfl_sync(kAll, id, q);
-      if (idq >= 0) {
-        const uint32_t* src = slots + static_cast<uint64_t>(idq) * W;
-        uint32_t* dst = sb + q * W;
-#pragma unroll
-        for (uint32_t b = 0; b < CB; ++b) {
-          const uint32_t c = lane + 32u * b;
-          if (c < pre_ch) cp_row16(reuse, dst + 4u * c, src + 4u * c);
-        }
-      }
-    }
-  };
-
-  // Bits saved by the matching words of lane q's row (summed over its
-  // headers), as in k_decompress_fast: rows of 8 or more segments take one
-  // header per lane and a warp reduction per row (warp-collective), shorter
-  // rows a walk by lane q.
-  auto saved_bits = [&](const uint32_t* sb) -> uint32_t {
-    auto seg_saved = [&](uint32_t H, uint32_t s) -> uint32_t {
-      uint32_t c = p * __popc(H);
-      if constexpr (TAB && NPL > 0) {
-#pragma unroll
-        for (int k = 0; k < NPL; ++k) c += pscale * (__popc(H & epl[s * NPL + k]) << k);
-      }
-      return c;
-    };
-    uint32_t mine = 0;
-    if constexpr (SC >= 8) {
-      constexpr uint32_t RPP = SC >= 32 ? 1u : 32u / SC;  // rows per pass
-      const uint32_t qo = SC >= 32 ? 0u : lane / SC;
-#pragma unroll
-      for (uint32_t q0 = 0; q0 < G; q0 += RPP) {
-        uint32_t c = 0;
-        if (q0 + qo < G) {
-          const uint32_t* hb = sb + (q0 + qo) * W;
-#pragma unroll
-          for (uint32_t s = SC >= 32 ? lane : lane % SC; s < SC; s += 32) c += seg_saved(hb[s], s);
-        }
-#pragma unroll
-        for (uint32_t r = 0; r < RPP; ++r) {
-          if (q0 + r >= G) break;
-          const uint32_t t = __reduce_add_sync(kAll, qo == r ? c : 0u);
-          if (lane == q0 + r) mine = t;
-        }
-      }
-    } else {
-      if (lane < G) {
-        const uint32_t* hb = sb + lane * W;
-        if constexpr (SC >= 4) {
-#pragma unroll
-          for (uint32_t s = 0; s < SC; s += 4) {
-            const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
-            mine += seg_saved(h.x, s) + seg_saved(h.y, s + 1) + seg_saved(h.z, s + 2) + seg_saved(h.w, s + 3);
-          }
-        } else {
-#pragma unroll
-          for (uint32_t s = 0; s < SC; ++s) mine += seg_saved(hb[s], s);
-        }
-      }
-    }
-    return mine;
-  };
-
-  // Warp-collective (saved_bits).
-  auto row_info = [&](const uint32_t* sb, int32_t id, uint32_t bmw, uint32_t& kind, uint32_t& nt) {
-    const uint32_t saved = saved_bits(sb);
-    kind = kNone;
-    nt = 0;
-    if (id == kNoRow) return;
-    if (id == kBadId) {
-      kind = kBadRange;
-      return;
-    }
-    if (!((bmw >> (static_cast<uint32_t>(id) & 31u)) & 1u)) {
-      kind = kRaw;
-      nt = W;
-      return;
-    }
-    const uint32_t Lw = (32u * (SC + W) - saved + 31u) >> 5;
-    if (Lw >= W) {
-      kind = kCorrupt;
-      return;
-    }
-    kind = kComp;
-    nt = Lw;
-  };
-
-  auto issue_rest = [&](uint32_t* sb, int32_t id, uint32_t kind, uint32_t nt) {
-    const bool need = (kind == kRaw || kind == kComp) && nt > pre;
-    for (uint32_t mk = __ballot_sync(kAll, need); mk; mk &= mk - 1) {
-      const uint32_t q = __ffs(mk) - 1;
-      const uint32_t ntq = __shfl_sync(kAll, nt, q);
-      const uint32_t* src = slots + static_cast<uint64_t>(__shfl_sync(kAll, id, q)) * W;
-      uint32_t* dst = sb + q * W;
-      for (uint32_t c = pre_ch + lane; c < ((ntq + 3u) >> 2); c += 32) cp_row16(reuse, dst + 4u * c, src + 4u * c);
-    }
+    return pp.check_id(ids[g.pos + lane]);
   };
 
   constexpr uint32_t NA = BF16 ? 2 * SPW : SPW;  // accumulators per lane
@@ -247,85 +113,21 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
 #pragma unroll
   for (uint32_t s = 0; s < NA; ++s) acc[s] = 0.0f;
   uint64_t cnt = 0;  // ids of the current bag seen so far
-  // add decoded word w (word lane + 32 (s_lo + s) of a row)
-  auto add_word = [&](uint32_t s, uint32_t w) {
+  // add decoded word w (word lane + 32 (s_lo + j) of a row)
+  auto add_word = [&](uint32_t j, uint32_t w) {
     if constexpr (BF16) {
-      acc[2 * s] = __fadd_rn(acc[2 * s], __uint_as_float(w << 16));
-      acc[2 * s + 1] = __fadd_rn(acc[2 * s + 1], __uint_as_float(w & 0xFFFF0000u));
+      acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(w << 16));
+      acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __uint_as_float(w & 0xFFFF0000u));
     } else {
-      acc[s] = __fadd_rn(acc[s], __uint_as_float(w));
+      acc[j] = __fadd_rn(acc[j], __uint_as_float(w));
     }
   };
-
-  auto add_row = [&](const uint32_t* pb) {
-    uint32_t base = 32u * SC + 32u * lane;
-    // segment s of the row, pooled into accumulator j
-    auto seg = [&](uint32_t H, uint32_t s, uint32_t j) {
-      uint32_t P = base - p * __popc(H & lt);
-      uint32_t step = 1024u - p * __popc(H);
-      if constexpr (TAB && NPL > 0) {
-        uint32_t e_lt = 0, e_all = 0;
-#pragma unroll
-        for (int k = 0; k < NPL; ++k) {
-          const uint32_t Ek = H & epl[s * NPL + k];
-          e_lt += __popc(Ek & lt) << k;
-          e_all += __popc(Ek) << k;
-        }
-        P -= pscale * e_lt;
-        step -= pscale * e_all;
-      }
-      const uint32_t* q = pb + (P >> 5);
-      const uint32_t v = __funnelshift_r(q[0], q[1], P);
-      uint32_t y;
-      if constexpr (TAB) {
-        const uint32_t* e = tab + (32u * s + lane) * EW;
-        const uint4 e0 = *reinterpret_cast<const uint4*>(e);
-        if constexpr (EW == 4) {
-          const uint32_t m2[2] = {e0.x, e0.y};
-          y = deposit_runs_packed<(R < 2 ? R : 2)>(v, m2, e0.z) | e0.w;
-        } else {
-          const uint4 e1 = *reinterpret_cast<const uint4*>(e + 4);
-          const uint32_t m4[4] = {e0.x, e0.y, e0.z, e0.w};
-          y = deposit_runs_packed<R>(v, m4, e1.x) | e1.y;
-        }
-      } else {
-        y = deposit_runs<R>(v, rm, rs) | bm;
-      }
-      add_word(j, (H & lanebit) ? y : v);
-      base += step;
-    };
-    if constexpr (CS > 1) {
-      // step over the fields of the segments before this warp's slice
-      for (uint32_t s = 0; s < s_lo; ++s) {
-        const uint32_t H = pb[s];
-        uint32_t step = 1024u - p * __popc(H);
-        if constexpr (TAB && NPL > 0) {
-          uint32_t e_all = 0;
-#pragma unroll
-          for (int k = 0; k < NPL; ++k) e_all += __popc(H & epl[s * NPL + k]) << k;
-          step -= pscale * e_all;
-        }
-        base += step;
-      }
-#pragma unroll
-      for (uint32_t j = 0; j < SPW; ++j) seg(pb[s_lo + j], s_lo + j, j);
-    } else if constexpr (SC >= 4) {
-#pragma unroll
-      for (uint32_t s = 0; s < SC; s += 4) {
-        const uint4 h = *reinterpret_cast<const uint4*>(pb + s);
-        seg(h.x, s, s);
-        seg(h.y, s + 1, s + 1);
-        seg(h.z, s + 2, s + 2);
-        seg(h.w, s + 3, s + 3);
-      }
-    } else {
-#pragma unroll
-      for (uint32_t s = 0; s < SC; ++s) seg(pb[s], s, s);
-    }
+  auto add_row = [&](const uint32_t* pb, uint32_t q, const typename Pipe::Bases& bases) {
+    pp.template decode_segments<SPW>(pb, pb, q, s_lo, bases, [&](uint32_t j, uint32_t y) { add_word(j, y); });
   };
 
   // Add group g's rows in order; the group that ends a bag writes it out.
-  auto consume = [&](const Grp& g, const uint32_t* sb, uint32_t kind) {
+  auto consume = [&](const Grp& g, const uint32_t* sb, uint32_t kind, const typename Pipe::Bases& bases) {
     const uint32_t comp = __ballot_sync(kAll, kind == kComp);
     const uint32_t raw = __ballot_sync(kAll, kind == kRaw);
     const bool bad = kind == kBadRange || kind == kCorrupt;
@@ -335,12 +137,12 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
       // uniform plan, every row compressed: straight-line code, so the rows'
       // decode work overlaps (the additions still follow the row order)
 #pragma unroll
-      for (uint32_t q = 0; q < G; ++q) add_row(sb + q * W);
+      for (uint32_t q = 0; q < G; ++q) add_row(sb + q * W, q, bases);
     } else {
 #pragma unroll
       for (uint32_t q = 0; q < G; ++q) {
         if ((comp >> q) & 1u) {
-          add_row(sb + q * W);
+          add_row(sb + q * W, q, bases);
         } else if ((raw >> q) & 1u) {
 #pragma unroll
           for (uint32_t j = 0; j < SPW; ++j) add_word(j, sb[q * W + 32u * (s_lo + j) + lane]);
@@ -386,33 +188,36 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   }
 #pragma unroll
   for (int i = 0; i < D - 1; ++i) {
-    issue_prefix(st[i], idr[i], bmr[i]);
+    pp.issue_prefix(st[i], idr[i], pp.row_pos(idr[i]), bmr[i]);
     cp_commit();
     if (i < D - 2) cp_commit();
   }
   cp_wait<2 * D - 4>();
   __syncwarp();
   uint32_t kind0, nt0;
-  row_info(st[0], idr[0], bmr[0], kind0, nt0);
-  issue_rest(st[0], idr[0], kind0, nt0);
+  typename Pipe::Bases bases0;
+  pp.row_info(st[0], idr[0], pp.row_pos(idr[0]), bmr[0], kind0, nt0, bases0);
+  pp.issue_rest(st[0], idr[0], pp.row_pos(idr[0]), kind0, nt0);
   cp_commit();
 
   while (gr[0].bag < n_bags) {
     gr[D] = next_group();
     idr[D] = load_id(gr[D]);
-    issue_prefix(st[D - 1], idr[D - 1], bmr[D - 1]);
+    pp.issue_prefix(st[D - 1], idr[D - 1], pp.row_pos(idr[D - 1]), bmr[D - 1]);
     cp_commit();
     cp_wait<2 * D - 4>();
     __syncwarp();
     uint32_t kind1, nt1;
-    row_info(st[1], idr[1], bmr[1], kind1, nt1);
-    issue_rest(st[1], idr[1], kind1, nt1);
+    typename Pipe::Bases bases1;
+    pp.row_info(st[1], idr[1], pp.row_pos(idr[1]), bmr[1], kind1, nt1, bases1);
+    pp.issue_rest(st[1], idr[1], pp.row_pos(idr[1]), kind1, nt1);
     cp_commit();
     cp_wait<2>();
     __syncwarp();
-    consume(gr[0], st[0], kind0);
+    consume(gr[0], st[0], kind0, bases0);
     __syncwarp();
     kind0 = kind1;
+    bases0 = bases1;
     uint32_t* const t = st[0];
 #pragma unroll
     for (int i = 0; i < D - 1; ++i) st[i] = st[i + 1];

@@ -26,13 +26,12 @@
 
 #include <cuda_runtime.h>
 
-#include "ibp_internal.cuh"
+#include "ibp_decode_pipe.cuh"
 
 namespace ibp {
 
 constexpr int kFastWarps = 8;
 constexpr int kFastStages = 3;  // shared-memory stages per warp (D >= 3)
-constexpr uint32_t kAll = 0xFFFFFFFFu;
 // Words per group (GW; rows per group G = GW / W, at least 1).  512 by
 // default; 256 for copies that also allocate in L1 (IBP_HINT_ROW_REUSE on
 // host-mapped slots): the smaller stages leave more of the SM's on-chip
@@ -45,30 +44,6 @@ constexpr uint32_t kGroupWordsReuse = 256;
 constexpr uint32_t kGroupWordsDev = 768;
 constexpr uint32_t kGroupWordsDevTable = 1024;
 
-// Words of a per-word table entry in shared memory: {run masks, packed run
-// shifts, Bitval & Mask}: 4 words for up to two runs, 8 for up to four.
-template <int R>
-struct TabEntry {
-  static constexpr uint32_t EW = R <= 2 ? 4u : 8u;
-};
-
-template <int SC, int R, int NPL, bool TAB>
-struct TabShape {
-  static constexpr uint32_t W = 32u * SC;
-  static constexpr uint32_t ENT = TAB ? W * TabEntry<R>::EW : 0u;
-  static constexpr uint32_t EPL = TAB && NPL > 0 ? ((SC * NPL + 31u) / 32u) * 32u : 0u;
-  static constexpr uint32_t WORDS = ENT + EPL;  // shared words before the warp stages
-};
-
-template <int SC, uint32_t GW>
-struct FastShape {
-  static constexpr uint32_t W = 32u * SC;
-  static constexpr uint32_t G = GW / W >= 1 ? GW / W : 1u;  // rows per group
-  static constexpr uint32_t STAGE = G * W + 32u;           // words per stage
-  static constexpr uint32_t CH = W / 4;                    // 16-byte chunks per row
-  static constexpr uint32_t CB = (CH + 31) / 32;           // chunk blocks of 32 per row
-};
-
 // PK = false: row r of the table is slots[r * W ..]; PK = true: the packed
 // layout, row r is slots[offsets[r] .. offsets[r + 1]) (its stored words
 // rounded up to 16 bytes), and a row whose stream would reach past that
@@ -78,38 +53,39 @@ struct FastShape {
 // plan y of a.plans (a device array of plan views).
 // CTAs per SM the register allocation is sized for, where that causes no
 // spills (measured on one GB300): uniform plans up to W = 1024 with 512-word
-// groups fit four (+1 % on dense and DLRM rows); with the larger groups of
-// device slots shared memory holds two, and a two-CTA budget leaves the
-// straight-line decode its registers; per-word-table plans up to W = 512 with
+// groups fit four (+1 % on dense and DLRM rows); with the 768-word groups of
+// device slots shared memory holds three, and a three-CTA budget (80
+// registers) keeps them all resident; per-word-table plans up to W = 512 with
 // at most one e-plane fit three with 512-word groups (instead of the two that
 // 107 registers allowed: +9 % for device slots, -2 % over the host link, so
 // host slots keep the compiler's choice) and two with 1024-word groups; other
 // shapes keep the compiler's choice.
-template <int SC, int NPL, bool TAB, bool MP, bool DEV, uint32_t GW>
+// Rows split into tasks (NP > 1) have small stages: three CTAs.
+template <int SC, int NPL, bool TAB, bool MP, bool DEV, uint32_t GW, int NP = 1>
 constexpr int fast_min_blocks() {
-  if (!TAB) return DEV ? 2 : (SC <= 32 ? 4 : 1);
+  if (NP > 1) return 3;
+  if (!TAB) return DEV ? (SC <= 32 ? 3 : 1) : (SC <= 32 ? 4 : 1);
   if (DEV && !MP && SC <= 16 && NPL <= 1) return GW >= 1024 ? 2 : 3;
   return 1;
 }
 
-// DEV only selects the register budget (fast_min_blocks).
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false>
-__global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV, GW>())) k_decompress_fast(const DecodeArgs a) {
+// DEV only selects the register budget (fast_min_blocks).  NP > 1: every row
+// is NP tasks of 16 segments (RowPipe), for rows of 32 or 64 segments whose
+// slots are in device memory.
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false, int NP = 1>
+__global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV, GW, NP>())) k_decompress_fast(const DecodeArgs a) {
   static_assert(!MP || (TAB && !PK), "plan sets decode through the table path, slot layout");
-  using F = FastShape<SC, GW>;
-  using T = TabShape<SC, R, NPL, TAB>;
+  static_assert(NP == 1 || !MP, "plan sets decode whole rows");
+  using Pipe = RowPipe<R, SC, NPL, TAB, PK, GW, NP>;
+  using F = typename Pipe::F;
+  using T = typename Pipe::T;
   constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
-  constexpr uint32_t EW = TabEntry<R>::EW;
   extern __shared__ __align__(128) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t nw_cta = blockDim.x >> 5;
-  uint32_t* const tab = smem;             // [W][EW] per-word entries (TAB)
-  uint32_t* const epl = smem + T::ENT;    // [SC][NPL] e-planes (TAB, NPL > 0)
   constexpr int D = kFastStages;
   uint32_t* const stages = smem + T::WORDS + warp * static_cast<uint32_t>(D) * STAGE;
-  const uint32_t lt = lanemask_lt();
-  const uint32_t lanebit = 1u << lane;
 
   // this CTA's plan, row range and output
   PlanView pv;
@@ -117,40 +93,14 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     pv = a.plans[blockIdx.y];
   else
     pv = a.pv;
-  const uint64_t n_out = MP ? a.rows_per_plan : a.n_out;
+  const uint64_t n_out = (MP ? a.rows_per_plan : a.n_out) * NP;  // rows, or tasks
   const uint64_t first = MP ? a.first + blockIdx.y * a.rows_per_plan : a.first;
   uint32_t* const out = MP ? a.out + blockIdx.y * a.rows_per_plan * (32ull * SC) : a.out;
 
-  // plan constants: uniform Mask (TAB = false) or the per-word tables
-  const uint32_t p = TAB ? pv.p_min : pv.u_p;
-  const uint32_t pscale = pv.p_scale;
-  const uint32_t bm = pv.u_bm;
-  uint32_t rm[R], rs[R];
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-    rm[k] = pv.u_rmask[k];
-    rs[k] = pv.u_rsh[k];
-  }
-  if constexpr (TAB) {
-    // Stage the tables once per CTA; every thread reaches this barrier
-    // before any warp leaves.
-    for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
-      uint32_t* e = tab + w * EW;
-#pragma unroll
-      for (int k = 0; k < (EW == 4 ? 2 : 4); ++k) e[k] = k < R ? __ldg(pv.rmask + k * W + w) : 0u;
-      e[EW == 4 ? 2 : 4] = __ldg(pv.rshift + w);
-      e[EW == 4 ? 3 : 5] = __ldg(pv.bm + w);
-    }
-    if constexpr (NPL > 0) {
-      for (uint32_t i = threadIdx.x; i < SC * NPL; i += blockDim.x)
-        epl[i] = __ldg(pv.eplanes + (i / NPL) * kPlanes + (i % NPL));
-    }
-    __syncthreads();
-  }
-  const bool reuse = (pv.hints & IBP_HINT_ROW_REUSE) != 0;
-  const uint32_t pre = MP ? pv.pre : a.pre;  // multiple of 4, <= W
-  const uint32_t pre_ch = pre >> 2;    // prefix chunks per row
-  const uint32_t n_rows32 = static_cast<uint32_t>(a.n_rows);  // < 2^31 (checked by the launcher)
+  // plan constants, and the per-word tables staged once per CTA (every
+  // thread reaches the barrier inside before any warp leaves)
+  Pipe pp;
+  pp.init(pv, a.slots, a.bitmask, a.offsets, a.n_rows, NP > 1 ? SC : (MP ? pv.pre : a.pre), smem);
 
   // Warp gw owns groups gw, gw + nwarps, ...; group g is output rows
   // g*G .. g*G + G - 1 and lane q < G owns row g*G + q.
@@ -169,213 +119,38 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
   const uint64_t J = (n_groups - gw + nwarps - 1) / nwarps;
   const uint64_t row_step = nwarps * G;  // first row of group j+1 minus first row of group j
 
-  // Row ids are carried as 32-bit values; -1 marks "no row" (past the end of
-  // the output) and kBadId an id outside [0, n_rows).
-  constexpr int32_t kNoRow = -1, kBadId = -2;
   auto load_id = [&](uint64_t j, uint64_t rbase) -> int32_t {
     const uint64_t i = rbase + lane;
     if (j >= J || lane >= G || i >= n_out) return kNoRow;
-    const int64_t id = a.ids ? a.ids[i] : static_cast<int64_t>(first + i);
-    return (id >= 0 && static_cast<uint64_t>(id) < n_rows32) ? static_cast<int32_t>(id) : kBadId;
+    const uint64_t r = i / NP;  // output row (NP > 1: of task i)
+    return pp.check_id(a.ids ? a.ids[r] : static_cast<int64_t>(first + r));
   };
+  // NP > 1: the part of its row that the task of group j (first task rbase) is
+  auto part_of = [&](uint64_t rbase) -> uint32_t { return static_cast<uint32_t>(rbase % NP); };
 
-  // Word offset of a row in the slots (PK: in the packed buffer) and the
-  // number of words it occupies there.
-  struct RowPos {
-    uint64_t off;
-    uint32_t ext;
-  };
-  auto row_pos = [&](int32_t id) -> RowPos {
-    if constexpr (PK) {
-      if (id < 0) return {0, 0};
-      const uint64_t lo = a.offsets[id], hi = a.offsets[id + 1];
-      const uint64_t ext = hi > lo ? hi - lo : 0;
-      return {lo, static_cast<uint32_t>(ext < W ? ext : W)};
-    } else {
-      return {static_cast<uint64_t>(id >= 0 ? id : 0) * W, W};
-    }
-  };
-
-  // Prefix of group j: lane i copies chunk i (+32 ...) of every row.
-  auto issue_prefix = [&](uint64_t j, uint32_t* sb, int32_t id, RowPos rp, uint32_t& bmw) {
-    if (id >= 0) bmw = ld_u32(a.bitmask + (static_cast<uint32_t>(id) >> 5));
-    if (j >= J) return;
-#pragma unroll
-    for (uint32_t q = 0; q < G; ++q) {
-      const int32_t idq = __shfl_sync(kAll, id, q);
-      uint64_t offq;
-      if constexpr (PK)
-        offq = __shfl_sync(kAll, static_cast<unsigned long long>(rp.off), q);
-      else
-        offq = static_cast<uint64_t>(idq) * W;
-      // PK: a row shorter than the prefix is corrupt (row_info says so) and
-      // is not read
-      bool ok = idq >= 0;
-      if constexpr (PK) ok = ok && __shfl_sync(kAll, rp.ext, q) >= pre;
-      if (ok) {
-        const uint32_t* src = a.slots + offq;
-        uint32_t* dst = sb + q * W;
-#pragma unroll
-        for (uint32_t b = 0; b < CB; ++b) {
-          const uint32_t c = lane + 32u * b;
-          if (c < pre_ch) cp_row16(reuse, dst + 4u * c, src + 4u * c);
-        }
-      }
-    }
-  };
-
-  // Bits that the matching words of a row save against 32 bits each (p per
-  // match, plus pscale * e for the e-planes of per-word plans), summed over
-  // its S headers.  Rows of 8 or more segments: one header per lane, G rows
-  // in ceil(G / (32 / SC)) passes, each row's sum by a warp reduction and
-  // kept by lane q for row q (warp-collective: every lane calls it).
-  // Shorter rows: lane q walks its own row's headers.
-  auto saved_bits = [&](const uint32_t* sb) -> uint32_t {
-    auto seg_saved = [&](uint32_t H, uint32_t s) -> uint32_t {
-      uint32_t c = p * __popc(H);
-      if constexpr (TAB && NPL > 0) {
-#pragma unroll
-        for (int k = 0; k < NPL; ++k) c += pscale * (__popc(H & epl[s * NPL + k]) << k);
-      }
-      return c;
-    };
-    uint32_t mine = 0;
-    if constexpr (SC >= 8) {
-      constexpr uint32_t RPP = SC >= 32 ? 1u : 32u / SC;  // rows per pass
-      const uint32_t qo = SC >= 32 ? 0u : lane / SC;       // this lane's row in a pass
-#pragma unroll
-      for (uint32_t q0 = 0; q0 < G; q0 += RPP) {
-        uint32_t c = 0;
-        if (q0 + qo < G) {
-          const uint32_t* hb = sb + (q0 + qo) * W;
-#pragma unroll
-          for (uint32_t s = SC >= 32 ? lane : lane % SC; s < SC; s += 32) c += seg_saved(hb[s], s);
-        }
-#pragma unroll
-        for (uint32_t r = 0; r < RPP; ++r) {
-          if (q0 + r >= G) break;
-          const uint32_t t = __reduce_add_sync(kAll, qo == r ? c : 0u);
-          if (lane == q0 + r) mine = t;
-        }
-      }
-    } else {
-      if (lane < G) {
-        const uint32_t* hb = sb + lane * W;
-        if constexpr (SC >= 4) {
-#pragma unroll
-          for (uint32_t s = 0; s < SC; s += 4) {
-            const uint4 h = *reinterpret_cast<const uint4*>(hb + s);
-            mine += seg_saved(h.x, s) + seg_saved(h.y, s + 1) + seg_saved(h.z, s + 2) + seg_saved(h.w, s + 3);
-          }
-        } else {
-#pragma unroll
-          for (uint32_t s = 0; s < SC; ++s) mine += seg_saved(hb[s], s);
-        }
-      }
-    }
-    return mine;
-  };
-
-  // Kind and stream length of lane q's row of group j (headers in stage).
-  // Warp-collective (saved_bits).
-  auto row_info = [&](const uint32_t* sb, int32_t id, RowPos rp, uint32_t bmw, uint32_t& kind,
-                      uint32_t& nt) {
-    const uint32_t saved = saved_bits(sb);
-    kind = kNone;
-    nt = 0;
-    if (id == kNoRow) return;
-    if (id == kBadId) {
-      kind = kBadRange;
+  // NP > 1: one task; its words WP * part .. of output row rbase / NP.
+  auto decode_task = [&](const uint32_t* sb, uint64_t rbase, uint32_t kind, uint32_t nt,
+                         const typename Pipe::Bases& bases) {
+    const uint32_t k0 = __shfl_sync(kAll, kind, 0);
+    if (k0 == kNone) return;
+    const uint32_t part = part_of(rbase);
+    uint32_t* const orow = out + (rbase / NP) * W + part * Pipe::WP;
+    if (k0 == kComp) {
+      const uint32_t c0 = __shfl_sync(kAll, nt, 0) >> 16;
+      uint32_t* const o = orow + lane;
+      pp.template decode_segments<Pipe::SEGP>(sb, sb, 0u, part * Pipe::SEGP, bases,
+                                              [&](uint32_t j, uint32_t y) { o[32u * j] = y; },
+                                              128u * c0 - 32u * SC);
       return;
     }
-    if (!((bmw >> (static_cast<uint32_t>(id) & 31u)) & 1u)) {
-      kind = (PK && rp.ext < W) ? kCorrupt : kRaw;
-      nt = kind == kRaw ? W : 0u;
-      return;
-    }
-    if (PK && rp.ext < pre) {
-      kind = kCorrupt;
-      return;
-    }
-    const uint32_t Lw = (32u * (SC + W) - saved + 31u) >> 5;
-    if (Lw >= W || (PK && ((Lw + 3u) & ~3u) > rp.ext)) {
-      kind = kCorrupt;
-      return;
-    }
-    kind = kComp;
-    nt = Lw;
+    if (k0 != kRaw && lane == 0) record_status(pv.status, k0 == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
+    const uint4* prow = reinterpret_cast<const uint4*>(sb + SC);
+#pragma unroll
+    for (uint32_t c = lane; c < Pipe::WP / 4; c += 32)
+      reinterpret_cast<uint4*>(orow)[c] = k0 == kRaw ? prow[c] : make_uint4(0, 0, 0, 0);
   };
 
-  // Rest of group j: [pre, Lw) of compressed rows, [pre, W) of raw rows.
-  auto issue_rest = [&](uint64_t j, uint32_t* sb, int32_t id, RowPos rp, uint32_t kind, uint32_t nt) {
-    if (j >= J) return;
-    const bool need = (kind == kRaw || kind == kComp) && nt > pre;
-    for (uint32_t mk = __ballot_sync(kAll, need); mk; mk &= mk - 1) {
-      const uint32_t q = __ffs(mk) - 1;
-      const uint32_t ntq = __shfl_sync(kAll, nt, q);
-      uint64_t offq;
-      if constexpr (PK)
-        offq = __shfl_sync(kAll, static_cast<unsigned long long>(rp.off), q);
-      else
-        offq = static_cast<uint64_t>(__shfl_sync(kAll, id, q)) * W;
-      const uint32_t* src = a.slots + offq;
-      uint32_t* dst = sb + q * W;
-      for (uint32_t c = pre_ch + lane; c < ((ntq + 3u) >> 2); c += 32) cp_row16(reuse, dst + 4u * c, src + 4u * c);
-    }
-  };
-
-  auto decode_row = [&](const uint32_t* pb, uint32_t* o) {
-    uint32_t base = 32u * SC + 32u * lane;
-    auto seg = [&](uint32_t H, uint32_t s) {
-      uint32_t P = base - p * __popc(H & lt);
-      uint32_t step = 1024u - p * __popc(H);
-      if constexpr (TAB && NPL > 0) {
-        uint32_t e_lt = 0, e_all = 0;
-#pragma unroll
-        for (int k = 0; k < NPL; ++k) {
-          const uint32_t Ek = H & epl[s * NPL + k];
-          e_lt += __popc(Ek & lt) << k;
-          e_all += __popc(Ek) << k;
-        }
-        P -= pscale * e_lt;
-        step -= pscale * e_all;
-      }
-      const uint32_t* q = pb + (P >> 5);
-      const uint32_t v = __funnelshift_r(q[0], q[1], P);
-      uint32_t y;
-      if constexpr (TAB) {
-        const uint32_t* e = tab + (32u * s + lane) * EW;
-        const uint4 e0 = *reinterpret_cast<const uint4*>(e);
-        if constexpr (EW == 4) {
-          const uint32_t m2[2] = {e0.x, e0.y};
-          y = deposit_runs_packed<(R < 2 ? R : 2)>(v, m2, e0.z) | e0.w;
-        } else {
-          const uint4 e1 = *reinterpret_cast<const uint4*>(e + 4);
-          const uint32_t m4[4] = {e0.x, e0.y, e0.z, e0.w};
-          y = deposit_runs_packed<R>(v, m4, e1.x) | e1.y;
-        }
-      } else {
-        y = deposit_runs<R>(v, rm, rs) | bm;
-      }
-      o[32u * s] = (H & lanebit) ? y : v;
-      base += step;
-    };
-    if constexpr (SC >= 4) {
-#pragma unroll
-      for (uint32_t s = 0; s < SC; s += 4) {
-        const uint4 h = *reinterpret_cast<const uint4*>(pb + s);
-        seg(h.x, s);
-        seg(h.y, s + 1);
-        seg(h.z, s + 2);
-        seg(h.w, s + 3);
-      }
-    } else {
-#pragma unroll
-      for (uint32_t s = 0; s < SC; ++s) seg(pb[s], s);
-    }
-  };
-
-  auto decode_group = [&](const uint32_t* sb, uint64_t rbase, uint32_t kind) {
+  auto decode_group = [&](const uint32_t* sb, uint64_t rbase, uint32_t kind, const typename Pipe::Bases& bases) {
     uint32_t* const obase = out + rbase * W + lane;
     const uint32_t comp = __ballot_sync(kAll, kind == kComp);
     const uint32_t raw = __ballot_sync(kAll, kind == kRaw);
@@ -387,11 +162,17 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
       // code, so the rows' independent offset chains and shared loads can
       // overlap
 #pragma unroll
-      for (uint32_t q = 0; q < G; ++q) decode_row(sb + q * W, obase + q * W);
+      for (uint32_t q = 0; q < G; ++q) {
+        uint32_t* o = obase + q * W;
+        pp.decode_row(sb + q * W, q, bases, [&](uint32_t s, uint32_t y) { o[32u * s] = y; });
+      }
     } else {
 #pragma unroll
       for (uint32_t q = 0; q < G; ++q) {
-        if ((comp >> q) & 1u) decode_row(sb + q * W, obase + q * W);
+        if ((comp >> q) & 1u) {
+          uint32_t* o = obase + q * W;
+          pp.decode_row(sb + q * W, q, bases, [&](uint32_t s, uint32_t y) { o[32u * s] = y; });
+        }
       }
     }
     if (raw | badm) {
@@ -433,37 +214,44 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
   for (int i = 0; i < D; ++i) {
     st[i] = stages + i * STAGE;
     bmr[i] = 0;
-    rpr[i] = row_pos(idr[i]);
+    rpr[i] = pp.row_pos(idr[i]);
   }
 #pragma unroll
   for (int i = 0; i < D - 1; ++i) {
-    issue_prefix(i, st[i], idr[i], rpr[i], bmr[i]);
+    if (static_cast<uint64_t>(i) < J) pp.issue_prefix(st[i], idr[i], rpr[i], bmr[i]);
     cp_commit();
     if (i < D - 2) cp_commit();
   }
   cp_wait<2 * D - 4>();
   __syncwarp();
   uint32_t kind0, nt0;
-  row_info(st[0], idr[0], rpr[0], bmr[0], kind0, nt0);
-  issue_rest(0, st[0], idr[0], rpr[0], kind0, nt0);
+  typename Pipe::Bases bases0;
+  pp.row_info(st[0], idr[0], rpr[0], bmr[0], kind0, nt0, bases0, part_of(rb0));
+  pp.issue_rest(st[0], idr[0], rpr[0], kind0, nt0);
   cp_commit();
 
   for (uint64_t j = 0; j < J; ++j, rb0 += row_step) {
     idr[IA] = load_id(j + IA, rb0 + IA * row_step);
-    if constexpr (PK) rpr[D] = row_pos(idr[D]);
-    issue_prefix(j + D - 1, st[D - 1], idr[D - 1], rpr[D - 1], bmr[D - 1]);
+    if constexpr (PK) rpr[D] = pp.row_pos(idr[D]);
+    if (j + D - 1 < J) pp.issue_prefix(st[D - 1], idr[D - 1], rpr[D - 1], bmr[D - 1]);
     cp_commit();
     cp_wait<2 * D - 4>();
     __syncwarp();
     uint32_t kind1, nt1;
-    row_info(st[1], idr[1], rpr[1], bmr[1], kind1, nt1);
-    issue_rest(j + 1, st[1], idr[1], rpr[1], kind1, nt1);
+    typename Pipe::Bases bases1;
+    pp.row_info(st[1], idr[1], rpr[1], bmr[1], kind1, nt1, bases1, part_of(rb0 + row_step));
+    if (j + 1 < J) pp.issue_rest(st[1], idr[1], rpr[1], kind1, nt1);
     cp_commit();
     cp_wait<2>();
     __syncwarp();
-    decode_group(st[0], rb0, kind0);
+    if constexpr (NP > 1)
+      decode_task(st[0], rb0, kind0, nt0, bases0);
+    else
+      decode_group(st[0], rb0, kind0, bases0);
     __syncwarp();
     kind0 = kind1;
+    nt0 = nt1;
+    bases0 = bases1;
     uint32_t* const t = st[0];
 #pragma unroll
     for (int i = 0; i < D - 1; ++i) st[i] = st[i + 1];
@@ -472,7 +260,7 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     for (int i = 0; i < IA; ++i) idr[i] = idr[i + 1];
 #pragma unroll
     for (int i = 0; i < D; ++i) rpr[i] = rpr[i + 1];
-    if constexpr (!PK) rpr[D - 1] = row_pos(idr[D - 1]);
+    if constexpr (!PK) rpr[D - 1] = pp.row_pos(idr[D - 1]);
 #pragma unroll
     for (int i = 0; i < D - 1; ++i) bmr[i] = bmr[i + 1];
     bmr[D - 1] = 0;
@@ -480,9 +268,9 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
   cp_wait<0>();
 }
 
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false>
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false, int NP = 1>
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  using F = FastShape<SC, GW>;
+  using F = FastShape<SC, GW, NP>;
   using T = TabShape<SC, R, NPL, TAB>;
   const size_t per_warp = 4ull * kFastStages * F::STAGE;
   const size_t fixed = 4ull * T::WORDS;
@@ -490,7 +278,7 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = fixed + warps * per_warp;
-  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW, MP, DEV>;
+  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW, MP, DEV, NP>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
   // for this launch shape.
   static int occ_cache[64] = {0};
@@ -513,7 +301,7 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
     }
     occ_cache[dev] = occ;
   }
-  const uint64_t groups = ((MP ? a.rows_per_plan : a.n_out) + F::G - 1) / F::G;
+  const uint64_t groups = ((MP ? a.rows_per_plan : a.n_out) * NP + F::G - 1) / F::G;
   const uint64_t need = (groups + warps - 1) / warps;
   uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);
   if (MP) cap = cap / a.n_plans > 0 ? cap / a.n_plans : 1;  // CTAs per plan
@@ -548,8 +336,9 @@ static int launch_fast_sc(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stre
     case 4: return launch_fast_t<R, 4, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
     case 8: return launch_fast_t<R, 8, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
     case 16: return launch_fast_t<R, 16, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
-    case 32: return launch_fast_t<R, 32, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
-    default: return launch_fast_t<R, 64, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
+    // rows of 32 and 64 segments in device memory: tasks of 16 segments
+    case 32: return launch_fast_t<R, 32, NPL, TAB, PK, GW, false, DEV, (DEV && !PK ? 2 : 1)>(plan, a, stream);
+    default: return launch_fast_t<R, 64, NPL, TAB, PK, GW, false, DEV, (DEV && !PK ? 4 : 1)>(plan, a, stream);
   }
 }
 
