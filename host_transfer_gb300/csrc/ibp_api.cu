@@ -75,10 +75,12 @@ int sm_count(int device) {
   return n;
 }
 
-// Makes `device` current for the lifetime of the guard.
+// Makes `device` current for the lifetime of the guard (and restores the
+// previous device only when it had to change it).
 struct DeviceGuard {
   int prev = -1;
   bool ok = true;
+  bool changed = false;
   explicit DeviceGuard(int device) {
     if (cudaGetDevice(&prev) != cudaSuccess) {
       ok = false;
@@ -91,11 +93,13 @@ struct DeviceGuard {
         ok = false;
         set_cuda_error(e, "cudaSetDevice");
         cudaGetLastError();
+      } else {
+        changed = true;
       }
     }
   }
   ~DeviceGuard() {
-    if (ok && prev >= 0) cudaSetDevice(prev);
+    if (changed) cudaSetDevice(prev);
   }
 };
 

@@ -150,8 +150,16 @@ def _word_rows(t: torch.Tensor):
     return ctypes.c_void_p(t.data_ptr()), n, W
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, device) -> ctypes.c_void_p:
+    """The cudaStream_t to launch on: `stream`, else torch's current stream of
+    `device` (read as a raw handle: no Stream object per call)."""
     if stream is None:
+        if _raw_stream is not None:
+            idx = device if isinstance(device, int) else torch.device(device).index
+            return ctypes.c_void_p(_raw_stream(torch.cuda.current_device() if idx is None else idx))
         stream = torch.cuda.current_stream(device)
     if isinstance(stream, torch.cuda.Stream):
         return ctypes.c_void_p(stream.cuda_stream)

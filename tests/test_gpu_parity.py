@@ -513,3 +513,36 @@ def test_wide_rows_in_hbm_split_into_tasks(W, shape):
     code = ibp.ibp_get_status(g["plan"], raise_on_error=False)
     st, ref = C.decompress(slots, g["bitmask"], np.arange(int(ok[0]), n), g["mask"], g["bitval"])
     assert code == st and np.array_equal(words_np(out), ref)
+
+
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_ids_and_status_word_in_pinned_host_memory(where):
+    """Row ids read by the kernel from pinned host memory (zero copy) give the
+    same rows as device ids, and ibp_get_status_async moves each call's status
+    into a pinned host word without a host wait: OK for a clean call, the data
+    error for a call with a bad id, cleared after it is moved."""
+    c = workloads.CONFIGS["tiny"]
+    rows = workloads.make_table("tiny")
+    g = gpu_codec(rows, rows[:256], c["T"], where)
+    bm = on_device(g["bitmask"])
+    n = rows.shape[0]
+    rng = np.random.default_rng(12)
+    ids = rng.integers(0, n, 5000).astype(np.int64)
+    ids_host = torch.from_numpy(ids).pin_memory()
+    words = torch.full((3,), -1, dtype=torch.int32, pin_memory=True)
+    out = ibp.ibp_gather_decompress(g["plan"], g["slots_t"], bm, ids_host)
+    ibp.ibp_get_status_async(g["plan"], words[0])
+    bad = torch.from_numpy(np.array([1, n + 3, 2], np.int64)).pin_memory()
+    out_bad = ibp.ibp_gather_decompress(g["plan"], g["slots_t"], bm, bad)
+    ibp.ibp_get_status_async(g["plan"], words[1])
+    ibp.ibp_get_status_async(g["plan"], words[2])
+    torch.cuda.synchronize()
+    assert words.tolist() == [ibp.IBP_OK, ibp.IBP_ERANGE, ibp.IBP_OK]
+    assert np.array_equal(words_np(out), rows[ids])
+    o = words_np(out_bad)
+    assert np.array_equal(o[[0, 2]], rows[[1, 2]]) and not o[1].any()
+    assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
+    # a device word works too
+    dword = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ibp.ibp_get_status_async(g["plan"], dword[0])
+    assert int(dword.item()) == ibp.IBP_OK
