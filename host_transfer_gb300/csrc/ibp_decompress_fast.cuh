@@ -175,6 +175,16 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
         }
       }
     }
+    if (raw == kGroupBits) {
+      // every row raw (e.g. K/V rows of 64 words that no Mask compresses): the
+      // group's rows are contiguous in the stage and in the output, so one
+      // flat copy in 16-byte chunks keeps every lane busy
+      const uint4* src = reinterpret_cast<const uint4*>(sb);
+      uint4* dst = reinterpret_cast<uint4*>(obase - lane);
+#pragma unroll
+      for (uint32_t c = lane; c < G * W / 4; c += 32) dst[c] = src[c];
+      return;
+    }
     if (raw | badm) {
       if (bad) record_status(pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
       for (uint32_t q = 0; q < G; ++q) {

@@ -128,11 +128,13 @@ def test_random_masks(W, runs):
         assert g["plan"].info["max_runs"] > 4
 
 
+@pytest.mark.parametrize("W", [32, 64, 512])
 @pytest.mark.parametrize("where", ["host", "hbm"])
-def test_mask_zero_all_raw(where):
-    """Sample rows that agree on nothing leave the Mask empty: every row raw."""
-    W = 64
-    rows = np.random.default_rng(1).integers(0, 2**32, (100, W), dtype=np.uint64).astype(np.uint32)
+def test_mask_zero_all_raw(where, W):
+    """Sample rows that agree on nothing leave the Mask empty: every row raw
+    (whole groups of raw rows are copied in one piece, the last partial group
+    row by row)."""
+    rows = np.random.default_rng(1).integers(0, 2**32, (101, W), dtype=np.uint64).astype(np.uint32)
     sample = np.stack([np.zeros(W, np.uint32), np.full(W, 0xFFFFFFFF, np.uint32)])
     g, _ = _check_codec(rows, sample, 1.0, where)
     assert not g["bitmask"].any() and g["plan"].info["max_kept_bits"] == 32
