@@ -384,13 +384,19 @@ def run_reference(args):
     name = "llm" if args.config in ("all", "llm") else args.config
     if name == "llm":
         L = args.layers
+        T = workloads.CONFIGS["llm"]["T"]
         used = sorted({s % L for s in range(WU + K)})
-        layers = dict(zip(used, [llm_layer(li) for li in used]))
+        pool_threads = max(1, min(16, os.cpu_count() or 1))
+        with ThreadPoolExecutor(pool_threads) as ex:  # generators and the C preprocess release the GIL
+            layers = dict(zip(used, ex.map(llm_layer, used)))
+            masks = {li: list(ex.map(lambda t: oracle_c.preprocess(llm_sample(li, t[1]), T), layers[li]))
+                     for li in used}
         comp = {}
         for li in used:
             comp[li] = []
-            for tname, tab in layers[li]:
-                slots, bitmask, m, b = oracle_compress_rows(tab, llm_sample(li, tab), workloads.CONFIGS["llm"]["T"])
+            for (tname, tab), (st, m, b) in zip(layers[li], masks[li]):
+                assert st == 0
+                slots, bitmask, _ = oracle_c.compress(tab, m, b)
                 comp[li].append((slots, bitmask, m, b, np.arange(tab.shape[0], dtype=np.int64)))
         step_bytes = sum(t.size * 4 for _, t in layers[used[0]])
         del layers
