@@ -377,16 +377,24 @@ struct RowPipe {
   template <uint32_t NS, class Sink>
   __device__ __forceinline__ void decode_segments(const uint32_t* hb, const uint32_t* pb, uint32_t q, uint32_t s_lo,
                                                   const Bases& bases, Sink&& sink, uint32_t bias = 0) const {
+    decode_segments_at<NS>(hb, pb, s_lo, [&](uint32_t j) { return seg_base(bases, q, s_lo + j) - bias; }, sink);
+  }
+
+  // As decode_segments, with base_of(j) giving the base of segment s_lo + j
+  // (warp-uniform), in stream bits of pb.
+  template <uint32_t NS, class BaseOf, class Sink>
+  __device__ __forceinline__ void decode_segments_at(const uint32_t* hb, const uint32_t* pb, uint32_t s_lo,
+                                                     BaseOf&& base_of, Sink&& sink) const {
     if constexpr (NS >= 4 && NS % 4 == 0) {
       if (s_lo % 4 == 0) {
 #pragma unroll
         for (uint32_t j = 0; j < NS; j += 4) {
           const uint4 h = *reinterpret_cast<const uint4*>(hb + s_lo + j);
           const uint32_t s = s_lo + j;
-          sink(j, decode_word(pb, h.x, s, seg_base(bases, q, s) - bias));
-          sink(j + 1, decode_word(pb, h.y, s + 1, seg_base(bases, q, s + 1) - bias));
-          sink(j + 2, decode_word(pb, h.z, s + 2, seg_base(bases, q, s + 2) - bias));
-          sink(j + 3, decode_word(pb, h.w, s + 3, seg_base(bases, q, s + 3) - bias));
+          sink(j, decode_word(pb, h.x, s, base_of(j)));
+          sink(j + 1, decode_word(pb, h.y, s + 1, base_of(j + 1)));
+          sink(j + 2, decode_word(pb, h.z, s + 2, base_of(j + 2)));
+          sink(j + 3, decode_word(pb, h.w, s + 3, base_of(j + 3)));
         }
         return;
       }
@@ -394,8 +402,21 @@ struct RowPipe {
 #pragma unroll
     for (uint32_t j = 0; j < NS; ++j) {
       const uint32_t s = s_lo + j;
-      sink(j, decode_word(pb, hb[s], s, seg_base(bases, q, s) - bias));
+      sink(j, decode_word(pb, hb[s], s, base_of(j)));
     }
+  }
+
+  // NP > 1: the bases of task `part`'s SEGP segments, less `bias`, gathered
+  // into one register (lane j holds segment part * SEGP + j's), so that each
+  // segment's base is one shuffle with a compile-time lane.
+  __device__ __forceinline__ uint32_t task_bases(const Bases& b, uint32_t part, uint32_t bias) const {
+    const uint32_t f = part * SEGP + (lane % SEGP);
+    uint32_t v;
+    if constexpr (NSEG > 32)
+      v = __shfl_sync(kAll, part * SEGP < 32 ? b.lo : b.hi, f & 31u);
+    else
+      v = __shfl_sync(kAll, b.lo, f);
+    return v - bias;
   }
 
   // The whole of row q: sink(s, y) gets word lane + 32 s, s = 0 .. SC-1.

@@ -138,9 +138,10 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     if (k0 == kComp) {
       const uint32_t c0 = __shfl_sync(kAll, nt, 0) >> 16;
       uint32_t* const o = orow + lane;
-      pp.template decode_segments<Pipe::SEGP>(sb, sb, 0u, part * Pipe::SEGP, bases,
-                                              [&](uint32_t j, uint32_t y) { o[32u * j] = y; },
-                                              128u * c0 - 32u * SC);
+      const uint32_t tb = pp.task_bases(bases, part, 128u * c0 - 32u * SC);
+      pp.template decode_segments_at<Pipe::SEGP>(
+          sb, sb, part * Pipe::SEGP, [&](uint32_t j) { return __shfl_sync(kAll, tb, j); },
+          [&](uint32_t j, uint32_t y) { o[32u * j] = y; });
       return;
     }
     if (k0 != kRaw && lane == 0) record_status(pv.status, k0 == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
