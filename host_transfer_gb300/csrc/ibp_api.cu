@@ -260,7 +260,7 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out) {
 }
 
 int ibp_plan_set_hints(ibp_plan* plan, uint32_t hints) {
-  if (!plan || (hints & ~IBP_HINT_ROW_REUSE)) return IBP_EINVAL;
+  if (!plan || (hints & ~(IBP_HINT_ROW_REUSE | IBP_HINT_EARLY_FETCH))) return IBP_EINVAL;
   plan->view.hints = hints;
   return IBP_OK;
 }

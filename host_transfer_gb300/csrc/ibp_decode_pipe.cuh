@@ -83,6 +83,7 @@ struct RowPipe {
   using T = TabShape<SC, R, NPL, TAB>;
   static constexpr uint32_t W = F::W, G = F::G, CB = F::CB;
   static constexpr uint32_t EW = TabEntry<R>::EW;
+  static constexpr uint32_t PCB = NP > 1 ? (SC / 4 + 31) / 32 : CB;  // chunk blocks a prefix can span
   static constexpr uint32_t SEGP = SC / NP;  // segments of a task
   static constexpr uint32_t WP = W / NP;     // output words of a task
   static_assert(NP == 1 || (!PK && SC >= 32 && SEGP == 16), "tasks of 16 segments, slot layout");
@@ -175,8 +176,11 @@ struct RowPipe {
       if (ok) {
         const uint32_t* src = slots + offq;
         uint32_t* dst = sb + q * W;
+        // blocks of 32 chunks up to the prefix's last (a task's prefix, its
+        // row's headers, is at most one block)
 #pragma unroll
-        for (uint32_t b = 0; b < CB; ++b) {
+        for (uint32_t b = 0; b < PCB; ++b) {
+          if (32u * b >= pre_ch) break;  // warp-uniform
           const uint32_t c = lane + 32u * b;
           if (c < pre_ch) cp_row16(reuse, dst + 4u * c, src + 4u * c);
         }

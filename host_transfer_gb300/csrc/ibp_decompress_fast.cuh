@@ -113,9 +113,14 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
   // memory visible, before touching per-call data (ids, bitmask, slots,
   // output, status).  The plan tables read above are written only when the
   // plan is created.  Without the launch attribute both are no-ops.
+  // IBP_HINT_EARLY_FETCH (the caller states that the previous kernel wrote
+  // none of this call's inputs): the wait moves after the pipeline's prologue,
+  // so the first ids and prefixes are fetched while the previous grid drains;
+  // every write still comes after the wait.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (gw >= n_groups) return;  // warp-uniform; only warp-level syncs below
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const bool early = (pv.hints & IBP_HINT_EARLY_FETCH) != 0;  // CTA-uniform
+  if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint64_t J = (n_groups - gw + nwarps - 1) / nwarps;
   const uint64_t row_step = nwarps * G;  // first row of group j+1 minus first row of group j
 
@@ -240,6 +245,7 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
   pp.row_info(st[0], idr[0], rpr[0], bmr[0], kind0, nt0, bases0, part_of(rb0));
   pp.issue_rest(st[0], idr[0], rpr[0], kind0, nt0);
   cp_commit();
+  if (early) asm volatile("griddepcontrol.wait;" ::: "memory");  // before the first write
 
   for (uint64_t j = 0; j < J; ++j, rb0 += row_step) {
     idr[IA] = load_id(j + IA, rb0 + IA * row_step);

@@ -36,6 +36,7 @@ IBP_ERANGE = 5
 IBP_ETIMEOUT = 6
 
 IBP_HINT_ROW_REUSE = 1
+IBP_HINT_EARLY_FETCH = 2
 
 _lib = None
 

@@ -47,7 +47,10 @@
  *   decompress kernels are launched as programmatic dependents: their blocks
  *   may be placed on the GPU while the previous kernel of the stream drains,
  *   but they read and write no per-call data (ids, slots, bitmask, outputs,
- *   status) before that kernel has completed, so stream order holds.
+ *   status) before that kernel has completed, so stream order holds.  (With
+ *   IBP_HINT_EARLY_FETCH set on the plan, the caller states that the previous
+ *   kernel wrote none of the inputs, and the reads may start earlier; see
+ *   ibp_plan_set_hints.)
  * - Alignment: slots, rows and outputs whose base is 16-byte aligned and whose
  *   W is a multiple of 4 take the 16-byte vector path; anything else takes a
  *   4-byte path with identical results.
@@ -68,7 +71,8 @@ extern "C" {
 #define IBP_NOALLOC_MAX_W 4096u
 
 /* Hints for ibp_plan_set_hints (bit flags). */
-#define IBP_HINT_ROW_REUSE 1u /* calls request the same rows repeatedly (skewed ids) */
+#define IBP_HINT_ROW_REUSE 1u   /* calls request the same rows repeatedly (skewed ids) */
+#define IBP_HINT_EARLY_FETCH 2u /* a call's inputs are not written by the kernel just before it */
 
 typedef enum ibp_status {
   IBP_OK = 0,       /* success */
@@ -186,13 +190,32 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out);
 
 /*
  * Access hints for the decompress calls made with this plan (a bit set of
- * IBP_HINT_*; 0 restores the default).  They change speed, never results.
+ * IBP_HINT_*; 0 restores the default).  IBP_HINT_ROW_REUSE changes speed,
+ * never results; IBP_HINT_EARLY_FETCH states a property of the caller's
+ * stream, and results are unchanged whenever that property holds.
  *
  * IBP_HINT_ROW_REUSE: the row ids of a call repeat a lot (skewed lookups such
  * as Zipf-distributed embedding ids).  Row copies then also allocate in the
  * SM's L1, so a repeat is served on chip instead of being fetched again over
  * the host link (mapped host memory is not kept in L2).  For ids without
  * repeats it costs a few percent, so it is off by default.
+ *
+ * IBP_HINT_EARLY_FETCH: the ids (and packed offsets), bitmask and slots that
+ * a gather- or contiguous-decompress call reads are not written by the kernel
+ * launched just before it on the same stream (they were written by the host,
+ * by a copy, or by an earlier kernel).  The decoder is launched as a
+ * programmatic dependent of that kernel, so its blocks can be placed on the
+ * GPU while that kernel drains; with this hint they already fetch their first
+ * ids and row prefixes there, instead of waiting for the kernel to complete,
+ * which hides a launch's start-up latency behind the previous launch's tail.
+ * Every write (output rows, status word) still waits for that kernel to
+ * complete, so a kernel that reads the previous call's output is unaffected.
+ * If the kernel just before does write the call's inputs, the call may read
+ * stale values: leave the hint off then (a copy or an event between the two
+ * is not a kernel and keeps full ordering).  Used by ibp_gather_decompress,
+ * ibp_decompress_contig, ibp_gather_decompress_packed and
+ * ibp_decompress_contig_set (each plan's hints as the set copied them);
+ * ignored by ibp_gather_decompress_bag.
  *
  * Takes effect for calls issued after it returns; not synchronised with
  * calls in flight.  Errors: IBP_EINVAL (NULL plan, unknown bits).

@@ -423,7 +423,7 @@ def test_row_reuse_hint_same_results(where):
     assert torch.equal(plain, hinted)
     assert np.array_equal(words_np(hinted), rows[ids])
     with pytest.raises(ibp.IbpError):
-        g["plan"].set_hints(2)
+        g["plan"].set_hints(4)  # no such hint
 
 
 @pytest.mark.parametrize("W", [32, 64, 128, 256, 512, 2048])

@@ -93,3 +93,37 @@ def test_stream_order_inside_a_captured_graph():
         assert np.array_equal(words_np(keep[k - 1]), want), k
         st, pw = B.embedding_bag(want, offsets.cpu().numpy(), B.SUM)
         assert st == 0 and np.array_equal(keep_bags[k - 1].cpu().numpy().view(np.uint32), pw), k
+
+
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_early_fetch_hint_keeps_results_when_inputs_are_ready(where):
+    """IBP_HINT_EARLY_FETCH: the decoder fetches its first ids and prefixes
+    while the previous kernel drains.  With inputs that no kernel just before
+    writes (here: set up before the loop), the results are those of the plain
+    calls, also when a kernel reads each call's output just after it and when
+    calls follow one another back to back on one stream."""
+    rows, g = _table(seed=3)
+    g_in = gpu_codec(rows, rows[:4000], 0.9, where)
+    plan, slots = g_in["plan"], g_in["slots_t"]
+    bm = on_device(g_in["bitmask"])
+    n = rows.shape[0]
+    rng = np.random.default_rng(4)
+    batches = [torch.from_numpy(rng.integers(0, n, 50000).astype(np.int64)).cuda() for _ in range(6)]
+    plan.set_hints(ibp.IBP_HINT_EARLY_FETCH)
+    outs, sums = [], []
+    for k in range(12):
+        out = ibp.ibp_gather_decompress(plan, slots, bm, batches[k % 6])
+        outs.append(out)
+        sums.append(out.view(torch.float32).sum(dim=1))  # a kernel reads the output just after
+    contig = [ibp.ibp_decompress_contig(plan, slots, bm, 17 * k, 4000) for k in range(4)]
+    torch.cuda.synchronize()
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+    for k, out in enumerate(outs):
+        want = rows[batches[k % 6].cpu().numpy()]
+        assert np.array_equal(words_np(out), want), k
+        assert torch.equal(sums[k], torch.from_numpy(want.view(np.float32)).cuda().sum(dim=1))
+    for k, out in enumerate(contig):
+        assert np.array_equal(words_np(out), rows[17 * k:17 * k + 4000]), k
+    plan.set_hints(0)
+    with pytest.raises(ibp.IbpError):
+        plan.set_hints(4)
