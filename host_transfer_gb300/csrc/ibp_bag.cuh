@@ -65,7 +65,11 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   const uint64_t team = gw / CS, nteams = nwarps / CS;  // warps per CTA are a multiple of CS
   const uint32_t s_lo = CS == 1 ? 0u : static_cast<uint32_t>(gw % CS) * SPW;
   if (team >= n_bags) return;  // warp-uniform; only warp-level syncs below
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // IBP_HINT_EARLY_FETCH: as in k_decompress_fast, the prologue's reads (bag
+  // offsets, ids, bitmask words, prefixes) may come before the wait; every
+  // write (pooled rows, status word) comes after it.
+  const bool early = (pv.hints & IBP_HINT_EARLY_FETCH) != 0;
+  if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- the cursor over this warp's bags (warp-uniform state) ----
   struct Grp {
@@ -199,6 +203,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   pp.row_info(st[0], idr[0], pp.row_pos(idr[0]), bmr[0], kind0, nt0, bases0);
   pp.issue_rest(st[0], idr[0], pp.row_pos(idr[0]), kind0, nt0);
   cp_commit();
+  if (early) asm volatile("griddepcontrol.wait;" ::: "memory");  // before the first write
 
   while (gr[0].bag < n_bags) {
     gr[D] = next_group();

@@ -200,8 +200,8 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out);
  * the host link (mapped host memory is not kept in L2).  For ids without
  * repeats it costs a few percent, so it is off by default.
  *
- * IBP_HINT_EARLY_FETCH: the ids (and packed offsets), bitmask and slots that
- * a gather- or contiguous-decompress call reads are not written by the kernel
+ * IBP_HINT_EARLY_FETCH: the ids (and packed or bag offsets), bitmask and slots
+ * that a decompress call reads are not written by the kernel
  * launched just before it on the same stream (they were written by the host,
  * by a copy, or by an earlier kernel).  The decoder is launched as a
  * programmatic dependent of that kernel, so its blocks can be placed on the
@@ -213,9 +213,9 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out);
  * If the kernel just before does write the call's inputs, the call may read
  * stale values: leave the hint off then (a copy or an event between the two
  * is not a kernel and keeps full ordering).  Used by ibp_gather_decompress,
- * ibp_decompress_contig, ibp_gather_decompress_packed and
- * ibp_decompress_contig_set (each plan's hints as the set copied them);
- * ignored by ibp_gather_decompress_bag.
+ * ibp_decompress_contig, ibp_gather_decompress_packed,
+ * ibp_gather_decompress_bag and ibp_decompress_contig_set (each plan's hints
+ * as the set copied them).
  *
  * Takes effect for calls issued after it returns; not synchronised with
  * calls in flight.  Errors: IBP_EINVAL (NULL plan, unknown bits).

@@ -116,6 +116,8 @@ def test_early_fetch_hint_keeps_results_when_inputs_are_ready(where):
         outs.append(out)
         sums.append(out.view(torch.float32).sum(dim=1))  # a kernel reads the output just after
     contig = [ibp.ibp_decompress_contig(plan, slots, bm, 17 * k, 4000) for k in range(4)]
+    offs = torch.arange(0, 50001, 50, dtype=torch.int64, device="cuda")
+    bags = [ibp.ibp_gather_decompress_bag(plan, slots, bm, batches[k], offs) for k in range(3)]
     torch.cuda.synchronize()
     assert ibp.ibp_get_status(plan) == ibp.IBP_OK
     for k, out in enumerate(outs):
@@ -124,6 +126,9 @@ def test_early_fetch_hint_keeps_results_when_inputs_are_ready(where):
         assert torch.equal(sums[k], torch.from_numpy(want.view(np.float32)).cuda().sum(dim=1))
     for k, out in enumerate(contig):
         assert np.array_equal(words_np(out), rows[17 * k:17 * k + 4000]), k
+    for k, out in enumerate(bags):
+        st, want = B.embedding_bag(rows[batches[k].cpu().numpy()], offs.cpu().numpy(), B.SUM)
+        assert st == 0 and np.array_equal(words_np(out), want), k
     plan.set_hints(0)
     with pytest.raises(ibp.IbpError):
         plan.set_hints(4)
