@@ -315,9 +315,13 @@ static int launch_bag_table(const ibp_plan* plan, BagArgs& a, cudaStream_t strea
 
 template <uint32_t GW, bool BF16, int CS = 1>
 static int launch_bag_gw(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
-  if (!plan->uniform)
+  if (!plan->uniform) {
+    if (plan->max_runs <= 1 && plan->view.npl <= 1)  // one-run deposits, as in the decoder
+      return plan->view.npl == 0 ? launch_bag_sc<1, 0, true, GW, BF16, CS>(plan, a, stream)
+                                 : launch_bag_sc<1, 1, true, GW, BF16, CS>(plan, a, stream);
     return plan->max_runs <= 2 ? launch_bag_table<2, GW, BF16, CS>(plan, a, stream)
                                : launch_bag_table<4, GW, BF16, CS>(plan, a, stream);
+  }
   switch (plan->max_runs) {
     case 1: return launch_bag_sc<1, 0, false, GW, BF16, CS>(plan, a, stream);
     case 2: return launch_bag_sc<2, 0, false, GW, BF16, CS>(plan, a, stream);

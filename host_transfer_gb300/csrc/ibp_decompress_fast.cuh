@@ -380,6 +380,11 @@ static int launch_table_r(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stre
 
 template <bool PK, uint32_t GW, bool DEV = false>
 static int launch_fast_table_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  // one run of kept bits per word and at most one e-plane (the sparse tables'
+  // plans): a one-run deposit per word instead of two
+  if (plan->max_runs <= 1 && plan->view.npl <= 1)
+    return plan->view.npl == 0 ? launch_fast_sc<1, 0, true, PK, GW, DEV>(plan, a, stream)
+                               : launch_fast_sc<1, 1, true, PK, GW, DEV>(plan, a, stream);
   return plan->max_runs <= 2 ? launch_table_r<2, PK, GW, DEV>(plan, a, stream)
                              : launch_table_r<4, PK, GW, DEV>(plan, a, stream);
 }
