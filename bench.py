@@ -678,27 +678,31 @@ def run_table(ctx: Ctx, name: str, cpu_seconds: float) -> dict:
     # Eager calls as a user makes them: every step's ids sit in pinned host
     # memory and the decode kernel reads them there (zero copy, like the
     # compressed rows), and the step's status word is moved into pinned host
-    # memory on a side stream once the decode has run; the host checks every
-    # step's word after the last step.  Two calls per step, and the compute
-    # stream carries the decodes back to back.  Run right after the
+    # memory by a status read enqueued right after the decode on the same
+    # stream; the host checks every step's word after the last step.  Two
+    # calls per step; the status read launches as a programmatic dependent, so
+    # consecutive decodes still overlap.  Run right after the
     # graph-timed leg, over the same steps, so that both see the host table in
     # the same state (the GPU's translations of its pages warm).
     ids_host = torch.from_numpy(batches).pin_memory()
     status_host = torch.full((WU + K,), -1, dtype=torch.int32, pin_memory=True)
-    side = torch.cuda.Stream(dev)
-    done = torch.cuda.Event()
     # set-up, untimed: the GPU's first access to newly pinned pages is slow, so
     # every batch's ids are read once by the kernel before any step
     for k in range(pool):
         ibp.ibp_gather_decompress(plan, table, bitmask, ids_host[k], out=out_of(k))
     ctx.sync()
 
+    # The per-step tensors (views of the pinned id and status buffers and of
+    # the output ring) are made once, as a pipeline that reuses its buffers
+    # holds them: building a view per call costs the host more than the call.
+    ids_v = [ids_host[k] for k in range(pool)]
+    out_v = [out_of(k) for k in range(ring_n)]
+    status_v = [status_host[k] for k in range(WU + K)]
+
     def e2e_step(s):
         # H2D: step s's ids and compressed rows, read by the kernel
-        ibp.ibp_gather_decompress(plan, table, bitmask, ids_host[s % pool], out=out_of(s), stream=stream)
-        done.record(stream)
-        side.wait_event(done)
-        ibp.ibp_get_status_async(plan, status_host[s], stream=side)  # D2H: step s's status
+        ibp.ibp_gather_decompress(plan, table, bitmask, ids_v[s % pool], out=out_v[s % ring_n], stream=stream)
+        ibp.ibp_get_status_async(plan, status_v[s], stream=stream)  # D2H: step s's status
 
     for s in range(WU):
         e2e_step(s)
@@ -819,7 +823,7 @@ def run_table(ctx: Ctx, name: str, cpu_seconds: float) -> dict:
                 "d2h_bytes_per_step": 4, "enqueue_ms_per_step": round(1e3 * enqueue_s / K, 4),
                 "what": "eager API calls; per step the ids and the compressed rows read from pinned host memory "
                         "by the kernel (the step's host-to-device bytes) and the status word moved into pinned host "
-                        "memory on a side stream; wall clock, one synchronisation at the end"},
+                        "memory by a status read on the same stream; wall clock, one synchronisation at the end"},
         "gpu_launches": K,
         "clocks": clocks,
         "table_gen_s": round(gen_s, 2),
@@ -919,22 +923,19 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
     # Eager calls: every step decodes one layer from its pinned host slots (the
     # kernels read the compressed bytes over the host link) and moves each
     # tensor's status word into pinned host memory, where the host checks them
-    # after the last step.  The status words come down on a side stream once
-    # the step's decodes have run, so the compute stream carries the decodes
-    # back to back.  Run right after the graph-timed leg, over the same layers,
+    # after the last step.  Each status read is enqueued right after its decode
+    # on the same stream; it launches as a programmatic dependent, so the
+    # decodes still overlap one another's start and drain.  Run right after the graph-timed leg, over the same layers,
     # so that both see the host slots in the same state (the GPU's translations
     # of their pages warm).
     status_host = torch.full((WU + K, 3), -1, dtype=torch.int32, pin_memory=True)
-    side = torch.cuda.Stream(dev)
-    done = torch.cuda.Event()
+
+    status_v = [[status_host[k, j] for j in range(3)] for k in range(WU + K)]  # views made once
 
     def e2e_step(s):
-        for e in layers[s % L]:
+        for e, word in zip(layers[s % L], status_v[s]):
             ibp.ibp_decompress_contig(e["plan"], e["host"], e["bitmask"], 0, e["n"], out=e["out"], stream=stream)
-        done.record(stream)
-        side.wait_event(done)
-        for j, e in enumerate(layers[s % L]):
-            ibp.ibp_get_status_async(e["plan"], status_host[s, j], stream=side)
+            ibp.ibp_get_status_async(e["plan"], word, stream=stream)  # D2H: this tensor's status
 
     for s in range(WU):
         e2e_step(s)
@@ -984,6 +985,7 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
                 blk = tab[h * seq:(h + 1) * seq]
                 sample = torch.from_numpy(llm_sample(li, blk).view(np.int32)).to(dev)
                 plan = ibp.ibp_plan_create(*ibp.ibp_preprocess(sample, c["T"]), device=ctx.local)
+                plan.set_hints(ibp.IBP_HINT_EARLY_FETCH)  # copied into the set below
                 ibp.ibp_compress(plan, host[h * seq:(h + 1) * seq],
                                  bitmask=bitmask[h * seq // 32:(h + 1) * seq // 32], stored=stw)
                 plans.append(plan)
@@ -1068,7 +1070,7 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
                 "d2h_bytes_per_step": 12, "enqueue_ms_per_step": round(1e3 * enqueue_s / K, 4),
                 "what": "eager API calls; per step one layer's compressed slots read from pinned host memory by "
                         "the kernels (the step's host-to-device bytes) and three status words moved into pinned "
-                        "host memory (side stream); wall clock, one synchronisation at the end"},
+                        "host memory by status reads on the same stream; wall clock, one synchronisation at the end"},
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "table_gen_s": round(gen_s, 2),

@@ -524,8 +524,16 @@ int ibp_get_status(const ibp_plan* plan, void* stream) {
 
 // Moves the status word to *dst and clears it, in one atomic exchange (so an
 // error recorded concurrently by another stream's kernel is either moved or
-// kept, never lost).
+// kept, never lost).  Launched as a programmatic dependent: it lets the next
+// kernel of the stream launch at once and then waits, before the exchange,
+// for the previous grid to complete with its memory visible.  A decode that
+// follows it on the same stream therefore still fetches its first ids and
+// prefixes while the previous decode drains; its own status writes come after
+// its wait, which ends only once this grid (and so the previous decode) has
+// completed.
 __global__ void k_take_status(uint32_t* status, uint32_t* dst) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) *dst = atomicExch(status, 0u);
 }
 
@@ -538,8 +546,22 @@ int ibp_get_status_async(const ibp_plan* plan, uint32_t* status_out, void* strea
   if (!g.ok) return IBP_ECUDA;
   const void* dst;
   if (resolve_ptr(status_out, plan->device, &dst)) return IBP_EINVAL;
-  k_take_status<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
-      plan->view.status, const_cast<uint32_t*>(static_cast<const uint32_t*>(dst)));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_take_status, plan->view.status,
+                                           const_cast<uint32_t*>(static_cast<const uint32_t*>(dst)));
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "k_take_status");
+    cudaGetLastError();
+    return IBP_ECUDA;
+  }
   return check_launch("k_take_status");
 }
 

@@ -148,27 +148,29 @@ def _word_rows(t: torch.Tensor):
     else:
         raise ValueError(f"unsupported dtype {t.dtype} / row length")
     n = (t.numel() * es) // (4 * W) if W else 0
-    return ctypes.c_void_p(t.data_ptr()), n, W
+    return t.data_ptr(), n, W
 
 
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
-def _stream(stream, device) -> ctypes.c_void_p:
-    """The cudaStream_t to launch on: `stream`, else torch's current stream of
-    `device` (read as a raw handle: no Stream object per call)."""
+def _stream(stream, device) -> int:
+    """The cudaStream_t to launch on, as a plain int: `stream`, else torch's
+    current stream of `device` (read as a raw handle: no Stream object per
+    call)."""
     if stream is None:
         if _raw_stream is not None:
             idx = device if isinstance(device, int) else torch.device(device).index
-            return ctypes.c_void_p(_raw_stream(torch.cuda.current_device() if idx is None else idx))
+            return _raw_stream(torch.cuda.current_device() if idx is None else idx)
         stream = torch.cuda.current_stream(device)
     if isinstance(stream, torch.cuda.Stream):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+    """A tensor's data pointer as a plain int (ctypes passes it as void*)."""
+    return t.data_ptr() if t is not None else None
 
 
 def _device_of(*ts) -> torch.device:

@@ -445,7 +445,11 @@ int ibp_get_status(const ibp_plan* plan, void* stream);
  * ordered before it (IBP_OK if none); read it after synchronising with the
  * stream (an event, cudaStreamSynchronize).  A caller can so check the result
  * of every decompress call without stopping the GPU between calls, e.g. one
- * word of a pinned ring per call, checked a few calls later.
+ * word of a pinned ring per call, checked a few calls later.  The kernel is
+ * launched as a programmatic dependent of the previous kernel of `stream` and
+ * lets the next one launch at once, so a status read between two decompress
+ * calls on one stream keeps their overlap (IBP_HINT_EARLY_FETCH): no event or
+ * side stream is needed to keep the decodes back to back.
  *
  * status_out  device-accessible uint32 (mapped pinned host memory, or device
  *             memory), owned by the caller; written by the kernel.

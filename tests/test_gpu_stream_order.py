@@ -132,3 +132,41 @@ def test_early_fetch_hint_keeps_results_when_inputs_are_ready(where):
     plan.set_hints(0)
     with pytest.raises(ibp.IbpError):
         plan.set_hints(4)
+
+
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_status_read_after_each_call_on_the_same_stream(where):
+    """ibp_get_status_async between back-to-back decodes on one stream (the
+    status kernel launches as a programmatic dependent, the decodes carry the
+    early-fetch hint and fill the GPU): every call's status word holds that
+    call's error and no other, and the rows are right."""
+    rows, g = _table(seed=5)
+    g_in = gpu_codec(rows, rows[:4000], 0.9, where)
+    plan, slots = g_in["plan"], g_in["slots_t"]
+    bm = on_device(g_in["bitmask"])
+    n = rows.shape[0]
+    rng = np.random.default_rng(6)
+    steps, bad_steps = 16, {3, 4, 11}
+    batches = []
+    for k in range(steps):
+        ids = rng.integers(0, n, 50000).astype(np.int64)
+        if k in bad_steps:
+            ids[-1] = n + k  # the last id of the batch, decoded by the grid's last groups
+        batches.append(torch.from_numpy(ids).pin_memory())
+    words = torch.full((steps,), -1, dtype=torch.int32, pin_memory=True)
+    plan.set_hints(ibp.IBP_HINT_EARLY_FETCH)
+    outs = []
+    for k in range(steps):
+        outs.append(ibp.ibp_gather_decompress(plan, slots, bm, batches[k]))
+        ibp.ibp_get_status_async(plan, words[k])
+    torch.cuda.synchronize()
+    plan.set_hints(0)
+    want_words = [ibp.IBP_ERANGE if k in bad_steps else ibp.IBP_OK for k in range(steps)]
+    assert words.tolist() == want_words
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+    for k, out in enumerate(outs):
+        ids = batches[k].numpy()
+        o = words_np(out)
+        good = ids < n
+        assert np.array_equal(o[good], rows[ids[good]]), k
+        assert not o[~good].any(), k
