@@ -77,7 +77,11 @@ struct RowPos {
   uint32_t ext;
 };
 
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, int NP = 1>
+// PAIR (rows of two or more segments): the decode of a compressed row gives
+// each lane two consecutive words of every 64-word block (decode_pairs_at),
+// written with one 8-byte store per lane; the per-word tables are then staged
+// in the order the lanes read them (see init).
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, int NP = 1, bool PAIR = false>
 struct RowPipe {
   using F = FastShape<SC, GW, NP>;
   using T = TabShape<SC, R, NPL, TAB>;
@@ -87,8 +91,10 @@ struct RowPipe {
   static constexpr uint32_t SEGP = SC / NP;  // segments of a task
   static constexpr uint32_t WP = W / NP;     // output words of a task
   static_assert(NP == 1 || (!PK && SC >= 32 && SEGP == 16), "tasks of 16 segments, slot layout");
+  static_assert(!PAIR || SC >= 2, "pairs need 64-word blocks");
 
   uint32_t lane, lt, lanebit;
+  uint32_t half, j0, plt, pbit0, pbit1;  // PAIR: segment 2k + half, positions j0, j0 + 1
   uint32_t p, pscale, bm;  // uniform: popcount(Mask), -, Bitval & Mask; tables: p_min, p_scale
   uint32_t rm[R], rs[R];   // uniform: runs of kept bits and their shifts
   const uint32_t* tab;     // shared: [W][EW] per-word entries (TAB)
@@ -108,6 +114,11 @@ struct RowPipe {
     lane = threadIdx.x & 31u;
     lt = lanemask_lt();
     lanebit = 1u << lane;
+    half = lane >> 4;
+    j0 = 2u * (lane & 15u);
+    plt = (1u << j0) - 1u;
+    pbit0 = 1u << j0;
+    pbit1 = pbit0 << 1;
     p = TAB ? pv.p_min : pv.u_p;
     pscale = pv.p_scale;
     bm = pv.u_bm;
@@ -120,7 +131,11 @@ struct RowPipe {
     epl = smem + T::ENT;
     if constexpr (TAB) {
       for (uint32_t w = threadIdx.x; w < W; w += blockDim.x) {
-        uint32_t* e = smem + w * EW;
+        // PAIR: word w = 64 k + 2 L + i (lane L, i = 0, 1) goes to entry
+        // 64 k + 32 i + L, so that the 32 lanes' reads of their i-th words are
+        // 32 consecutive entries
+        const uint32_t slot = PAIR ? ((w & ~63u) | ((w & 1u) << 5) | ((w & 63u) >> 1)) : w;
+        uint32_t* e = smem + slot * EW;
 #pragma unroll
         for (int k = 0; k < (EW == 4 ? 2 : 4); ++k) e[k] = k < R ? __ldg(pv.rmask + k * W + w) : 0u;
         e[EW == 4 ? 2 : 4] = __ldg(pv.rshift + w);
@@ -408,6 +423,85 @@ struct RowPipe {
       const uint32_t s = s_lo + j;
       sink(j, decode_word(pb, hb[s], s, base_of(j)));
     }
+  }
+
+  // PAIR: segments [s_lo, s_lo + NS) of a compressed row as NS / 2 blocks of
+  // 64 words.  In block k lane L rebuilds positions j0 = 2 (L mod 16) and
+  // j0 + 1 of segment s_lo + 2k + L / 16, i.e. words 2L and 2L + 1 of the
+  // block: its first field starts at the segment's base plus the bits of the
+  // segment's words below j0 (a popcount of the header, as in decode_word),
+  // and its second field right after the first (32 bits on, less what the
+  // first word saves if it matches: p, plus p_scale times its e-plane
+  // value, all from registers, so that both fields' reads issue at once).
+  // sink(k, y0, y1) receives the two words.  base_of(j) gives the base of
+  // segment s_lo + j (j differs between the two half-warps), in stream bits
+  // of pb; s_lo is even.
+  template <uint32_t NS, class BaseOf, class Sink>
+  __device__ __forceinline__ void decode_pairs_at(const uint32_t* hb, const uint32_t* pb, uint32_t s_lo,
+                                                  BaseOf&& base_of, Sink&& sink) const {
+    static_assert(NS % 2 == 0, "whole blocks");
+#pragma unroll
+    for (uint32_t k = 0; k < NS / 2; ++k) {
+      const uint32_t s = s_lo + 2u * k + half;
+      const uint32_t H = hb[s];
+      uint32_t P0 = base_of(2u * k + half) + 32u * j0 - p * __popc(H & plt);
+      uint32_t sv0 = p;  // bits the first word saves if it matches
+      if constexpr (TAB && NPL > 0) {
+        uint32_t e_lt = 0, e0 = 0;
+#pragma unroll
+        for (int kk = 0; kk < NPL; ++kk) {
+          const uint32_t E = epl[s * NPL + kk];
+          e_lt += __popc(H & E & plt) << kk;
+          e0 |= ((E >> j0) & 1u) << kk;
+        }
+        P0 -= pscale * e_lt;
+        sv0 += pscale * e0;
+      }
+      const uint32_t P1 = P0 + 32u - ((H & pbit0) ? sv0 : 0u);
+      uint32_t y[2];
+#pragma unroll
+      for (uint32_t i = 0; i < 2; ++i) {
+        const uint32_t P = i == 0 ? P0 : P1;
+        const uint32_t* q = pb + (P >> 5);
+        const uint32_t v = __funnelshift_r(q[0], q[1], P);
+        uint32_t d;
+        if constexpr (TAB) {
+          const uint32_t* e = tab + (64u * (s_lo / 2u + k) + 32u * i + lane) * EW;
+          const uint4 e0 = *reinterpret_cast<const uint4*>(e);
+          if constexpr (EW == 4) {
+            const uint32_t m2[2] = {e0.x, e0.y};
+            d = deposit_runs_packed<(R < 2 ? R : 2)>(v, m2, e0.z) | e0.w;
+          } else {
+            const uint4 e1 = *reinterpret_cast<const uint4*>(e + 4);
+            const uint32_t m4[4] = {e0.x, e0.y, e0.z, e0.w};
+            d = deposit_runs_packed<R>(v, m4, e1.x) | e1.y;
+          }
+        } else {
+          d = deposit_runs<R>(v, rm, rs) | bm;
+        }
+        y[i] = (H & (i == 0 ? pbit0 : pbit1)) ? d : v;
+      }
+      sink(k, y[0], y[1]);
+    }
+  }
+
+  // PAIR: the whole of row q; sink(k, y0, y1) gets words 64 k + 2 lane and
+  // 64 k + 2 lane + 1.
+  template <class Sink>
+  __device__ __forceinline__ void decode_row_pairs(const uint32_t* pb, uint32_t q, const Bases& bases,
+                                                   Sink&& sink) const {
+    decode_pairs_at<SC>(pb, pb, 0u, [&](uint32_t j) { return seg_base_pair(bases, q, j); }, sink);
+  }
+
+  // PAIR: the base of segment j of row q where j = 2k + half differs between
+  // the half-warps; both segments of a block sit in the same 32 lanes of the
+  // scan (f is even for the block's first), so the register is warp-uniform.
+  __device__ __forceinline__ uint32_t seg_base_pair(const Bases& b, uint32_t q, uint32_t j) const {
+    const uint32_t f = q * SC + j;
+    if constexpr (NSEG > 32)
+      return __shfl_sync(kAll, (f & ~1u) < 32 ? b.lo : b.hi, f & 31u);
+    else
+      return __shfl_sync(kAll, b.lo, f);
   }
 
   // NP > 1: the bases of task `part`'s SEGP segments, less `bias`, gathered

@@ -43,6 +43,17 @@ constexpr uint32_t kGroupWordsReuse = 256;
 // plans 1024 (sparse HBM 2167 -> 2299 GB/s: two 512-word rows per group).
 constexpr uint32_t kGroupWordsDev = 768;
 constexpr uint32_t kGroupWordsDevTable = 1024;
+// Compressed rows of two or more segments under per-word tables are rebuilt
+// two consecutive words per lane and written with 8-byte stores (RowPipe's
+// PAIR decode): one header popcount, one base shuffle and one store per two
+// words (sparse rows from HBM 2869 -> 2948 GB/s, packed 0.383 -> 0.400 of the
+// HBM peak).  Uniform plans keep one word per lane and segment: there a
+// half-warp's fields sit one segment after the other's (56 words for dense
+// rows), their shared-memory reads conflict two ways, and the pairs measured
+// no faster on dense rows (2938 -> 2904 GB/s) and slower on DLRM rows
+// (2849 -> 2748 GB/s).
+constexpr bool kPairUniform = false;
+constexpr bool kPairTable = true;
 
 // PK = false: row r of the table is slots[r * W ..]; PK = true: the packed
 // layout, row r is slots[offsets[r] .. offsets[r + 1]) (its stored words
@@ -76,7 +87,8 @@ template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = fals
 __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV, GW, NP>())) k_decompress_fast(const DecodeArgs a) {
   static_assert(!MP || (TAB && !PK), "plan sets decode through the table path, slot layout");
   static_assert(NP == 1 || !MP, "plan sets decode whole rows");
-  using Pipe = RowPipe<R, SC, NPL, TAB, PK, GW, NP>;
+  constexpr bool PAIR = SC >= 2 && (TAB ? kPairTable : kPairUniform);
+  using Pipe = RowPipe<R, SC, NPL, TAB, PK, GW, NP, PAIR>;
   using F = typename Pipe::F;
   using T = typename Pipe::T;
   constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
@@ -142,11 +154,18 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     uint32_t* const orow = out + (rbase / NP) * W + part * Pipe::WP;
     if (k0 == kComp) {
       const uint32_t c0 = __shfl_sync(kAll, nt, 0) >> 16;
-      uint32_t* const o = orow + lane;
       const uint32_t tb = pp.task_bases(bases, part, 128u * c0 - 32u * SC);
-      pp.template decode_segments_at<Pipe::SEGP>(
-          sb, sb, part * Pipe::SEGP, [&](uint32_t j) { return __shfl_sync(kAll, tb, j); },
-          [&](uint32_t j, uint32_t y) { o[32u * j] = y; });
+      if constexpr (PAIR) {
+        uint2* const o2 = reinterpret_cast<uint2*>(orow) + lane;
+        pp.template decode_pairs_at<Pipe::SEGP>(
+            sb, sb, part * Pipe::SEGP, [&](uint32_t j) { return __shfl_sync(kAll, tb, j); },
+            [&](uint32_t k, uint32_t y0, uint32_t y1) { o2[32u * k] = make_uint2(y0, y1); });
+      } else {
+        uint32_t* const o = orow + lane;
+        pp.template decode_segments_at<Pipe::SEGP>(
+            sb, sb, part * Pipe::SEGP, [&](uint32_t j) { return __shfl_sync(kAll, tb, j); },
+            [&](uint32_t j, uint32_t y) { o[32u * j] = y; });
+      }
       return;
     }
     if (k0 != kRaw && lane == 0) record_status(pv.status, k0 == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
@@ -163,22 +182,28 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     const bool bad = kind == kBadRange || kind == kCorrupt;
     const uint32_t badm = __ballot_sync(kAll, bad);
     constexpr uint32_t kGroupBits = G >= 32 ? kAll : (1u << G) - 1u;
+    // row q of the group, compressed: one 4-byte store per lane and segment,
+    // or (PAIR) one 8-byte store per lane and 64-word block
+    auto decode_comp = [&](uint32_t q) {
+      if constexpr (PAIR) {
+        uint2* const o2 = reinterpret_cast<uint2*>(obase - lane + q * W) + lane;
+        pp.decode_row_pairs(sb + q * W, q, bases,
+                            [&](uint32_t k, uint32_t y0, uint32_t y1) { o2[32u * k] = make_uint2(y0, y1); });
+      } else {
+        uint32_t* o = obase + q * W;
+        pp.decode_row(sb + q * W, q, bases, [&](uint32_t s, uint32_t y) { o[32u * s] = y; });
+      }
+    };
     if (!TAB && comp == kGroupBits) {
       // uniform plan, every row compressed (the common case): straight-line
       // code, so the rows' independent offset chains and shared loads can
       // overlap
 #pragma unroll
-      for (uint32_t q = 0; q < G; ++q) {
-        uint32_t* o = obase + q * W;
-        pp.decode_row(sb + q * W, q, bases, [&](uint32_t s, uint32_t y) { o[32u * s] = y; });
-      }
+      for (uint32_t q = 0; q < G; ++q) decode_comp(q);
     } else {
 #pragma unroll
       for (uint32_t q = 0; q < G; ++q) {
-        if ((comp >> q) & 1u) {
-          uint32_t* o = obase + q * W;
-          pp.decode_row(sb + q * W, q, bases, [&](uint32_t s, uint32_t y) { o[32u * s] = y; });
-        }
+        if ((comp >> q) & 1u) decode_comp(q);
       }
     }
     if (raw == kGroupBits) {

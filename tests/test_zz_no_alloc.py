@@ -115,3 +115,30 @@ def test_noalloc_rejects_rows_above_its_limit():
     m = torch.empty(IBP_NOALLOC_MAX_W + 1, dtype=torch.int32, device="cuda")
     assert _call(lib, "ibp_preprocess_noalloc", sample, 0.9, m, m.clone()) == ibp.IBP_EINVAL
     assert b"IBP_NOALLOC_MAX_W" in lib.ibp_last_error_detail()
+
+
+def test_noalloc_call_captured_in_a_graph():
+    """After a first call outside any capture, a call is captured in a CUDA
+    graph; replays on new samples written into the same buffer give the
+    oracle's Mask and Bitval each time (each replay clears its counters)."""
+    lib = ibp.load()
+    W, n, T = 256, 1500, 0.9
+    sample = _sample(6, n, W)
+    m = torch.empty(W, dtype=torch.int32, device="cuda")
+    b = torch.empty_like(m)
+    assert _call(lib, "ibp_preprocess_noalloc", sample, T, m, b) == ibp.IBP_OK
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rc = _call(lib, "ibp_preprocess_noalloc", sample, T, m, b)
+    assert rc == ibp.IBP_OK
+    for seed in (7, 8):
+        sample.copy_(_sample(seed, n, W))
+        m.fill_(-1)
+        b.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        st, mo, bo = C.preprocess(sample.cpu().numpy().view(np.uint32), T)
+        assert st == 0
+        assert np.array_equal(m.cpu().numpy().view(np.uint32), mo), seed
+        assert np.array_equal(b.cpu().numpy().view(np.uint32), bo), seed
