@@ -628,6 +628,8 @@ int ibp_gather_decompress_bag(const ibp_plan* plan, const uint32_t* slots, uint6
       resolve_ptr(bag_offsets, plan->device, &doff) || resolve_ptr(out, plan->device, &dout))
     return IBP_EINVAL;
   if (row_ids && resolve_ptr(row_ids, plan->device, &dids)) return IBP_EINVAL;
+  // bfloat16 rows: the pooled pairs of floats are written with 8-byte stores
+  if ((mode & IBP_BAG_BF16) && (reinterpret_cast<uintptr_t>(dout) & 7u)) return IBP_EINVAL;
   BagArgs a{};
   DecodeArgs& d = a.d;
   d.pv = plan->view;

@@ -39,7 +39,13 @@ namespace ibp {
 template <int R, int SC, int NPL, bool TAB, uint32_t GW, bool BF16, int CS = 1>
 __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   static_assert(CS >= 1 && SC % CS == 0, "a warp pools whole segments");
-  using Pipe = RowPipe<R, SC, NPL, TAB, false, GW>;
+  constexpr uint32_t SPW = SC / CS;  // segments this warp pools
+  // per-word tables: two consecutive words per lane (as in k_decompress_fast)
+  // where a warp pools whole rows (sparse bags from host slots 967 -> 979-984
+  // GB/s); warps of a team keep one word per lane (with pairs, sparse bags
+  // from HBM in teams of two: 2196 -> 1981 GB/s)
+  constexpr bool PAIR = TAB && kPairTable && CS == 1 && SPW % 2 == 0;
+  using Pipe = RowPipe<R, SC, NPL, TAB, false, GW, 1, PAIR>;
   using F = typename Pipe::F;
   using T = typename Pipe::T;
   constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE;
@@ -61,7 +67,6 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
   // may start as this grid drains; wait for the previous grid before
   // touching per-call data.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  constexpr uint32_t SPW = SC / CS;  // segments this warp pools
   const uint64_t team = gw / CS, nteams = nwarps / CS;  // warps per CTA are a multiple of CS
   const uint32_t s_lo = CS == 1 ? 0u : static_cast<uint32_t>(gw % CS) * SPW;
   if (team >= n_bags) return;  // warp-uniform; only warp-level syncs below
@@ -117,7 +122,12 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
 #pragma unroll
   for (uint32_t s = 0; s < NA; ++s) acc[s] = 0.0f;
   uint64_t cnt = 0;  // ids of the current bag seen so far
-  // add decoded word w (word lane + 32 (s_lo + j) of a row)
+  // Word j of this lane (j < SPW) is word lane + 32 (s_lo + j) of a row, or
+  // (PAIR) word 64 (j / 2) + 2 lane + j % 2 of segments s_lo ...
+  auto word_of = [&](uint32_t j) -> uint32_t {
+    return PAIR ? 32u * s_lo + 64u * (j / 2u) + 2u * lane + (j % 2u) : lane + 32u * (s_lo + j);
+  };
+  // add decoded word w (this lane's word j of a row)
   auto add_word = [&](uint32_t j, uint32_t w) {
     if constexpr (BF16) {
       acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(w << 16));
@@ -127,7 +137,16 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
     }
   };
   auto add_row = [&](const uint32_t* pb, uint32_t q, const typename Pipe::Bases& bases) {
-    pp.template decode_segments<SPW>(pb, pb, q, s_lo, bases, [&](uint32_t j, uint32_t y) { add_word(j, y); });
+    if constexpr (PAIR) {
+      pp.template decode_pairs_at<SPW>(
+          pb, pb, s_lo, [&](uint32_t j) { return pp.seg_base_pair(bases, q, s_lo + j); },
+          [&](uint32_t k, uint32_t y0, uint32_t y1) {
+            add_word(2u * k, y0);
+            add_word(2u * k + 1u, y1);
+          });
+    } else {
+      pp.template decode_segments<SPW>(pb, pb, q, s_lo, bases, [&](uint32_t j, uint32_t y) { add_word(j, y); });
+    }
   };
 
   // Add group g's rows in order; the group that ends a bag writes it out.
@@ -149,7 +168,7 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
           add_row(sb + q * W, q, bases);
         } else if ((raw >> q) & 1u) {
 #pragma unroll
-          for (uint32_t j = 0; j < SPW; ++j) add_word(j, sb[q * W + 32u * (s_lo + j) + lane]);
+          for (uint32_t j = 0; j < SPW; ++j) add_word(j, sb[q * W + word_of(j)]);
         }
       }
     }
@@ -159,16 +178,16 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
       const float c = static_cast<float>(cnt);
       const bool div = ba.mean && cnt;
       if constexpr (BF16) {
-        float2* const o = reinterpret_cast<float2*>(ba.out + g.bag * (2 * W)) + lane + 32u * s_lo;
+        float2* const o = reinterpret_cast<float2*>(ba.out + g.bag * (2 * W));
 #pragma unroll
         for (uint32_t j = 0; j < SPW; ++j) {
           const float lo = acc[2 * j], hi = acc[2 * j + 1];
-          o[32u * j] = div ? make_float2(__fdiv_rn(lo, c), __fdiv_rn(hi, c)) : make_float2(lo, hi);
+          o[word_of(j)] = div ? make_float2(__fdiv_rn(lo, c), __fdiv_rn(hi, c)) : make_float2(lo, hi);
         }
       } else {
-        float* const o = ba.out + g.bag * W + lane + 32u * s_lo;
+        float* const o = ba.out + g.bag * W;
 #pragma unroll
-        for (uint32_t j = 0; j < SPW; ++j) o[32u * j] = div ? __fdiv_rn(acc[j], c) : acc[j];
+        for (uint32_t j = 0; j < SPW; ++j) o[word_of(j)] = div ? __fdiv_rn(acc[j], c) : acc[j];
       }
 #pragma unroll
       for (uint32_t s = 0; s < NA; ++s) acc[s] = 0.0f;

@@ -226,3 +226,48 @@ def test_few_large_bags_from_hbm(W, n_bags):
         assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
         st, want = _expected(g, ids, offsets, mode)
         assert st == 0 and np.array_equal(out.cpu().numpy().view(np.uint32), want)
+
+
+@pytest.mark.parametrize("W", [64, 256])
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_bag_bf16_per_word_plan(W, where):
+    """bfloat16 rows under per-word Masks (every third element on a scale a
+    thousand times smaller): the table decoder's two words per lane pooled as
+    four floats, in bag order, against the oracle."""
+    from host_transfer_gb300 import workloads
+
+    rng = np.random.default_rng(700 + W)
+    n = 900
+    scale = np.where(np.arange(2 * W) % 3 == 0, 1e-3, 1.0)
+    x = (rng.normal(0, 1, (n, 2 * W)) * scale).astype(np.float32)
+    rows = workloads.bf16_pairs_to_words(workloads.f32_to_bf16_bits(x))
+    g = gpu_codec(rows, rows[:600], 0.95, where)
+    assert g["plan"].info["uniform"] == 0
+    ids = rng.integers(0, n, 2500).astype(np.int64)
+    offsets = _bags(rng, len(ids), max(1, 512 // W))
+    for mode in (ibp.IBP_BAG_SUM, ibp.IBP_BAG_MEAN):
+        out = ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]),
+                                            torch.from_numpy(ids).cuda(), torch.from_numpy(offsets).cuda(),
+                                            mode | ibp.IBP_BAG_BF16)
+        assert ibp.ibp_get_status(g["plan"]) == ibp.IBP_OK
+        st, dec = C.decompress(words_np(g["slots_t"]), g["bitmask"], ids, g["mask"], g["bitval"])
+        _, want = B.embedding_bag(dec, offsets, mode, bf16=True)
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), want)
+
+
+def test_bag_bf16_output_must_be_8_byte_aligned():
+    """bfloat16 bags are written as pairs of floats: an output that is only
+    4-byte aligned is refused before anything runs."""
+    rng = np.random.default_rng(5)
+    rows = _rows(rng, 128, 64)
+    g = gpu_codec(rows, rows, 0.9, "hbm")
+    ids = torch.zeros(4, dtype=torch.int64, device="cuda")
+    off = torch.tensor([0, 4], dtype=torch.int64, device="cuda")
+    buf = torch.zeros(2 * 128 + 1, dtype=torch.float32, device="cuda")
+    with pytest.raises(ibp.IbpError):
+        ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]), ids, off,
+                                      mode=ibp.IBP_BAG_BF16, out=buf[1:])
+    ok = ibp.ibp_gather_decompress_bag(g["plan"], g["slots_t"], on_device(g["bitmask"]), ids, off,
+                                       mode=ibp.IBP_BAG_BF16, out=buf[:-1])
+    torch.cuda.synchronize()
+    assert ok.data_ptr() == buf.data_ptr()

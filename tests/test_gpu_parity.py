@@ -377,12 +377,14 @@ def _run_mask(lo, length):
     return ((1 << length) - 1) << lo
 
 
-@pytest.mark.parametrize("W", [32, 128, 512])
+@pytest.mark.parametrize("W", [32, 64, 128, 512, 1024])
 @pytest.mark.parametrize("kind", ["same_popcount", "two_popcounts", "many_popcounts", "up_to_4_runs"])
 def test_per_word_plans_fast_table_modes(W, kind):
     """Per-word Masks of the shapes the table kernel specialises for: the same
     popcount at different positions (no e-plane), two popcounts (one e-plane),
-    many popcounts (six e-planes), and up to four runs of kept bits."""
+    many popcounts (six e-planes), and up to four runs of kept bits.  W = 32
+    decodes one word per lane; wider rows two words per lane (64-word blocks);
+    W = 1024 from device slots as tasks of 16 segments."""
     rng = np.random.default_rng(W + len(kind))
     keep = np.zeros(W, np.uint64)
     for w in range(W):
