@@ -156,9 +156,9 @@ __global__ void __launch_bounds__(kFastWarps * 32) k_bag(const BagArgs ba) {
     const bool bad = kind == kBadRange || kind == kCorrupt;
     if (bad) record_status(pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
     constexpr uint32_t kGroupBits = G >= 32 ? kAll : (1u << G) - 1u;
-    if (!TAB && comp == kGroupBits) {
-      // uniform plan, every row compressed: straight-line code, so the rows'
-      // decode work overlaps (the additions still follow the row order)
+    if ((!TAB || (kStraightTable && R <= 2)) && comp == kGroupBits) {
+      // every row compressed: straight-line code, so the rows' decode work
+      // overlaps (the additions still follow the row order)
 #pragma unroll
       for (uint32_t q = 0; q < G; ++q) add_row(sb + q * W, q, bases);
     } else {
