@@ -43,11 +43,14 @@ constexpr uint32_t kGroupWordsReuse = 256;
 // plans 1024 (sparse HBM 2167 -> 2299 GB/s: two 512-word rows per group).
 constexpr uint32_t kGroupWordsDev = 768;
 constexpr uint32_t kGroupWordsDevTable = 1024;
-// Compressed rows of two or more segments under per-word tables are rebuilt
-// two consecutive words per lane and written with 8-byte stores (RowPipe's
-// PAIR decode): one header popcount, one base shuffle and one store per two
-// words (sparse rows from HBM 2869 -> 2948 GB/s, packed 0.383 -> 0.400 of the
-// HBM peak).  Uniform plans keep one word per lane and segment: there a
+// Compressed rows of two or more segments under per-word tables, from device
+// memory (slots or the packed cache), are rebuilt two consecutive words per
+// lane and written with 8-byte stores (RowPipe's PAIR decode): one header
+// popcount, one base shuffle and one store per two words (sparse rows from
+// HBM 2869 -> 2948 GB/s, packed 0.383 -> 0.400 of the HBM peak; with the
+// straight-line group decode below, 0.58 -> 0.62 against one word per lane).
+// Decodes that wait on the host link keep one word per lane and the fewer
+// registers that allows.  Uniform plans keep one word per lane and segment: there a
 // half-warp's fields sit one segment after the other's (56 words for dense
 // rows), their shared-memory reads conflict two ways, and the pairs measured
 // no faster on dense rows (2938 -> 2904 GB/s) and slower on DLRM rows
@@ -58,8 +61,12 @@ constexpr bool kPairTable = true;
 // per-row branch), so the rows' offset chains and shared-memory loads overlap:
 // always for uniform plans, and for per-word tables of at most two runs per
 // word (sparse rows from HBM, two rows per group: 2957 -> 3476 GB/s, 0.53 ->
-// 0.62 of the HBM peak; packed 0.47 -> 0.51).  Tables of up to four runs keep
-// the per-row branch: straight-line code there spilled registers.
+// 0.62 of the HBM peak; packed 0.47 -> 0.51), on device slots only.  Tables of
+// up to four runs keep the per-row branch (straight-line code there spilled
+// registers), and so do host slots and plan sets: their decode waits on the
+// link, and the straight-line groups of up to eight rows took more registers
+// (80 -> 135) and so fewer CTAs (per-head K/V plan sets from host slots
+// 227 -> 174 GB/s).
 constexpr bool kStraightTable = true;
 
 // PK = false: row r of the table is slots[r * W ..]; PK = true: the packed
@@ -94,7 +101,7 @@ template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = fals
 __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV, GW, NP>())) k_decompress_fast(const DecodeArgs a) {
   static_assert(!MP || (TAB && !PK), "plan sets decode through the table path, slot layout");
   static_assert(NP == 1 || !MP, "plan sets decode whole rows");
-  constexpr bool PAIR = SC >= 2 && (TAB ? kPairTable : kPairUniform);
+  constexpr bool PAIR = SC >= 2 && (TAB ? kPairTable && DEV : kPairUniform);
   using Pipe = RowPipe<R, SC, NPL, TAB, PK, GW, NP, PAIR>;
   using F = typename Pipe::F;
   using T = typename Pipe::T;
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
         pp.decode_row(sb + q * W, q, bases, [&](uint32_t s, uint32_t y) { o[32u * s] = y; });
       }
     };
-    if ((!TAB || (kStraightTable && R <= 2)) && comp == kGroupBits) {
+    if ((!TAB || (kStraightTable && R <= 2 && DEV && !MP)) && comp == kGroupBits) {
       // every row compressed (the common case): straight-line code, so the
       // rows' independent offset chains and shared loads can overlap
 #pragma unroll
