@@ -54,9 +54,9 @@ struct TabShape {
 // NP > 1 (rows of 32 or 64 segments whose slots are in device memory): each
 // row is NP tasks of SC / NP segments, and a group is one task.  A task's
 // stage holds the row's S header words and then only the part of the stream
-// that its segments' fields occupy (at most 512 words plus alignment), so
-// stages stay small and more warps fit on an SM; each task re-reads the
-// row's headers.
+// that its segments' fields occupy (at most W / NP words plus alignment), so
+// stages stay smaller than a row's and more warps fit on an SM; each task
+// re-reads the row's headers.
 template <int SC, uint32_t GW, int NP = 1>
 struct FastShape {
   static constexpr uint32_t W = 32u * SC;
@@ -90,7 +90,7 @@ struct RowPipe {
   static constexpr uint32_t PCB = NP > 1 ? (SC / 4 + 31) / 32 : CB;  // chunk blocks a prefix can span
   static constexpr uint32_t SEGP = SC / NP;  // segments of a task
   static constexpr uint32_t WP = W / NP;     // output words of a task
-  static_assert(NP == 1 || (!PK && SC >= 32 && SEGP == 16), "tasks of 16 segments, slot layout");
+  static_assert(NP == 1 || (!PK && SC >= 32 && (SEGP == 16 || SEGP == 32)), "tasks of 16 or 32 segments, slot layout");
   static_assert(!PAIR || SC >= 2, "pairs need 64-word blocks");
 
   uint32_t lane, lt, lanebit;

@@ -85,7 +85,9 @@ constexpr bool kStraightTable = true;
 // 107 registers allowed: +9 % for device slots, -2 % over the host link, so
 // host slots keep the compiler's choice) and two with 1024-word groups; other
 // shapes keep the compiler's choice.
-// Rows split into tasks (NP > 1) have small stages: three CTAs.
+// Rows split into tasks (NP > 1): a register budget for three CTAs (tasks of
+// 32 segments, whose stages leave two CTAs per SM, measured the same with a
+// budget for two).
 template <int SC, int NPL, bool TAB, bool MP, bool DEV, uint32_t GW, int NP = 1>
 constexpr int fast_min_blocks() {
   if (NP > 1) return 3;
@@ -95,8 +97,8 @@ constexpr int fast_min_blocks() {
 }
 
 // DEV only selects the register budget (fast_min_blocks).  NP > 1: every row
-// is NP tasks of 16 segments (RowPipe), for rows of 32 or 64 segments whose
-// slots are in device memory.
+// is NP tasks of SC / NP segments (RowPipe), for rows of 32 or 64 segments
+// whose slots are in device memory.
 template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false, int NP = 1>
 __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV, GW, NP>())) k_decompress_fast(const DecodeArgs a) {
   static_assert(!MP || (TAB && !PK), "plan sets decode through the table path, slot layout");
@@ -391,9 +393,13 @@ static int launch_fast_sc(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stre
     case 4: return launch_fast_t<R, 4, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
     case 8: return launch_fast_t<R, 8, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
     case 16: return launch_fast_t<R, 16, NPL, TAB, PK, GW, false, DEV>(plan, a, stream);
-    // rows of 32 and 64 segments in device memory: tasks of 16 segments
+    // rows of 32 and 64 segments in device memory: two tasks per row (of 16
+    // and 32 segments; 2048-word rows in four tasks of 16: 13.3 us per LLM
+    // weight launch from HBM, in two of 32: 11.9 us, and the layer step 0.81
+    // -> 0.94 of the HBM peak, the next launches' CTAs finding room beside
+    // the two CTAs per SM that the larger stages leave)
     case 32: return launch_fast_t<R, 32, NPL, TAB, PK, GW, false, DEV, (DEV && !PK ? 2 : 1)>(plan, a, stream);
-    default: return launch_fast_t<R, 64, NPL, TAB, PK, GW, false, DEV, (DEV && !PK ? 4 : 1)>(plan, a, stream);
+    default: return launch_fast_t<R, 64, NPL, TAB, PK, GW, false, DEV, (DEV && !PK ? 2 : 1)>(plan, a, stream);
   }
 }
 

@@ -384,7 +384,7 @@ def test_per_word_plans_fast_table_modes(W, kind):
     popcount at different positions (no e-plane), two popcounts (one e-plane),
     many popcounts (six e-planes), and up to four runs of kept bits.  W = 32
     decodes one word per lane; wider rows two words per lane (64-word blocks);
-    W = 1024 from device slots as tasks of 16 segments."""
+    W = 1024 from device slots as two tasks of 16 segments."""
     rng = np.random.default_rng(W + len(kind))
     keep = np.zeros(W, np.uint64)
     for w in range(W):
@@ -474,8 +474,9 @@ def test_hbm_long_batches(W):
 @pytest.mark.parametrize("W", [1024, 2048])
 @pytest.mark.parametrize("shape", ["learned", "per_word"])
 def test_wide_rows_in_hbm_split_into_tasks(W, shape):
-    """Rows of 32 or 64 segments with slots in HBM are decoded as tasks of 16
-    segments, each from its row's headers and its own slice of the stream:
+    """Rows of 32 or 64 segments with slots in HBM are decoded as two tasks per
+    row (of 16 or 32 segments), each from its row's headers and its own slice
+    of the stream:
     compressed, raw, corrupt rows and bad ids, gathered and contiguous, all
     equal to the oracle's decode of the same slots."""
     rng = np.random.default_rng(W + len(shape))
