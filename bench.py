@@ -296,38 +296,70 @@ def llm_sample(li: int, tab: np.ndarray) -> np.ndarray:
 # path; here it is the reported baseline)
 
 
-def oracle_compress_rows(rows, sample, T):
-    """The oracle's own Mask/Bitval from `sample` and its slots of `rows`."""
+def oracle_compress_rows(rows, sample, T, timing=None):
+    """The oracle's own Mask/Bitval from `sample` and its slots of `rows`;
+    `timing` (a list) collects (bytes of rows, seconds) of the compress."""
     from oracle import oracle_c
 
     st, m, b = oracle_c.preprocess(sample, T)
     assert st == 0
+    t0 = time.perf_counter()
     slots, bitmask, _ = oracle_c.compress(rows, m, b)
+    if timing is not None:
+        timing.append((rows.size * 4, time.perf_counter() - t0))
     return slots, bitmask, m, b
 
 
-def cpu_table_baseline(rows, sample, T, id_batches, seconds, threads):
-    """The C oracle decoding `id_batches` (ids into `rows`) for about
-    `seconds`, on slots it compressed itself.  Returns (GB/s of uncompressed
-    output, ids decoded, seconds)."""
+def _decode_for(slots, bitmask, m, b, ids_of, seconds):
+    """The C oracle decoding id chunks ids_of(k), k = 0, 1, ..., until about
+    `seconds` have been spent; returns (ids decoded, seconds)."""
     from oracle import oracle_c
 
-    oracle_c.set_threads(threads)
-    remap = id_batches.reshape(-1)
-    slots, bitmask, m, b = oracle_compress_rows(rows, sample, T)
-    W = rows.shape[1]
-    chunk = 8192
-    nchunks = max(1, remap.size // chunk)
     done, used, k = 0, 0.0, 0
     while used < seconds:
-        ids = remap[(k % nchunks) * chunk:(k % nchunks + 1) * chunk]
+        ids = ids_of(k)
         t0 = time.perf_counter()
         st, _ = oracle_c.decompress(slots, bitmask, ids, m, b)
         used += time.perf_counter() - t0
         assert st == 0
         done += len(ids)
         k += 1
-    return done * 4 * W / used / 1e9, done, used
+    return done, used
+
+
+def cpu_extras(gbs1, secs1, comp, threads):
+    """The single-thread decode rate and the compress rate of the oracle."""
+    nbytes = sum(n for n, _ in comp)
+    csecs = sum(t for _, t in comp)
+    return {"single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"the same decode on one thread for {secs1:.1f} s"},
+            "compress": {"value": round(nbytes / csecs / 1e9, 4), "unit": "GB/s of input rows", "cores": threads,
+                         "sample": f"{nbytes / 1e6:.0f} MB of rows compressed once by the C oracle in "
+                                   f"{csecs:.2f} s (OpenMP over rows)"}}
+
+
+def cpu_table_baseline(rows, sample, T, id_batches, seconds, threads):
+    """The C oracle decoding `id_batches` (ids into `rows`) for about
+    `seconds` on all `threads`, and for a quarter of that on one thread, on
+    slots it compressed itself.  Returns (GB/s of uncompressed output, ids
+    decoded, seconds, extras: the single-thread and compress rates)."""
+    from oracle import oracle_c
+
+    oracle_c.set_threads(threads)
+    remap = id_batches.reshape(-1)
+    comp = []
+    slots, bitmask, m, b = oracle_compress_rows(rows, sample, T, comp)
+    W = rows.shape[1]
+    chunk = 8192
+    nchunks = max(1, remap.size // chunk)
+    ids_of = lambda k: remap[(k % nchunks) * chunk:(k % nchunks + 1) * chunk]  # noqa: E731
+    done, used = _decode_for(slots, bitmask, m, b, ids_of, seconds)
+    oracle_c.set_threads(1)
+    one = lambda k: remap[(k * 512) % max(1, remap.size - 512):][:512]  # noqa: E731
+    done1, used1 = _decode_for(slots, bitmask, m, b, one, seconds / 4)
+    oracle_c.set_threads(threads)
+    extras = cpu_extras(done1 * 4 * W / used1 / 1e9, used1, comp, threads)
+    return done * 4 * W / used / 1e9, done, used, extras
 
 
 def cpu_llm_baseline(layer, seconds, threads):
@@ -336,9 +368,9 @@ def cpu_llm_baseline(layer, seconds, threads):
     from oracle import oracle_c
 
     oracle_c.set_threads(threads)
-    comp = []
+    comp, timing = [], []
     for name, tab in layer:
-        slots, bitmask, m, b = oracle_compress_rows(tab, llm_sample(0, tab), 0.99)
+        slots, bitmask, m, b = oracle_compress_rows(tab, llm_sample(0, tab), 0.99, timing)
         comp.append((slots, bitmask, m, b, np.arange(tab.shape[0], dtype=np.int64)))
     step_bytes = sum(t.size * 4 for _, t in layer)
     done, used = 0, 0.0
@@ -349,7 +381,14 @@ def cpu_llm_baseline(layer, seconds, threads):
             assert st == 0
         used += time.perf_counter() - t0
         done += 1
-    return done * step_bytes / used / 1e9, done, used
+    # one thread: the weight rows, 64 at a time
+    oracle_c.set_threads(1)
+    slots, bitmask, m, b, ids = comp[0]
+    W = layer[0][1].shape[1]
+    done1, used1 = _decode_for(slots, bitmask, m, b, lambda k: ids[(64 * k) % (len(ids) - 64):][:64], seconds / 4)
+    oracle_c.set_threads(threads)
+    extras = cpu_extras(done1 * 4 * W / used1 / 1e9, used1, timing, threads)
+    return done * step_bytes / used / 1e9, done, used, extras
 
 
 # ---------------------------------------------------------------------------
@@ -846,11 +885,11 @@ def run_table(ctx: Ctx, name: str, cpu_seconds: float) -> dict:
     if ctx.cpu_ok:
         threads = os.cpu_count() or 1
         remap = np.searchsorted(cpu_keep, batches[:2])  # the two batches' ids into the kept rows
-        gbs, nids, secs = cpu_table_baseline(cpu_rows, cpu_sample, c["T"], remap, cpu_seconds, threads)
+        gbs, nids, secs, extras = cpu_table_baseline(cpu_rows, cpu_sample, c["T"], remap, cpu_seconds, threads)
         res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                "sample": f"{nids} ids of two of the bench's batches decoded by the bit-by-bit "
                                          f"C oracle in {secs:.1f} s (OpenMP over rows), on slots it compressed "
-                                         f"itself"}
+                                         f"itself", **extras}
     del table, ring
     return res
 
@@ -1079,11 +1118,11 @@ def run_llm(ctx: Ctx, cpu_seconds: float) -> dict:
     }
     if ctx.cpu_ok:
         threads = os.cpu_count() or 1
-        gbs, nl, secs = cpu_llm_baseline(originals[0], cpu_seconds, threads)
+        gbs, nl, secs, extras = cpu_llm_baseline(originals[0], cpu_seconds, threads)
         res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                "sample": f"layer 0 (weight, K, V) compressed by the oracle itself and decoded "
                                          f"{nl} times by the bit-by-bit C oracle in {secs:.1f} s "
-                                         f"(OpenMP over rows)"}
+                                         f"(OpenMP over rows)", **extras}
     return res
 
 
