@@ -50,11 +50,11 @@ constexpr uint32_t kGroupWordsDevTable = 1024;
 // HBM 2869 -> 2948 GB/s, packed 0.383 -> 0.400 of the HBM peak; with the
 // straight-line group decode below, 0.58 -> 0.62 against one word per lane).
 // Decodes that wait on the host link keep one word per lane and the fewer
-// registers that allows.  Uniform plans keep one word per lane and segment: there a
-// half-warp's fields sit one segment after the other's (56 words for dense
-// rows), their shared-memory reads conflict two ways, and the pairs measured
-// no faster on dense rows (2938 -> 2904 GB/s) and slower on DLRM rows
-// (2849 -> 2748 GB/s).
+// registers that allows.  Uniform plans keep one word per lane and segment:
+// there a half-warp's fields sit one segment after the other's (56 words for
+// dense rows), their shared-memory reads conflict two ways, and the pairs
+// measured no faster on dense rows (2938 -> 2904 GB/s) and slower on DLRM
+// rows (2849 -> 2748 GB/s).
 constexpr bool kPairUniform = false;
 constexpr bool kPairTable = true;
 // A group whose rows are all compressed is decoded as straight-line code (no
@@ -96,7 +96,9 @@ constexpr int fast_min_blocks() {
   return 1;
 }
 
-// DEV only selects the register budget (fast_min_blocks).  NP > 1: every row
+// DEV (slots or packed cache in device memory) selects the register budget
+// (fast_min_blocks) and, for per-word tables, the pair decode and the
+// straight-line groups.  NP > 1: every row
 // is NP tasks of SC / NP segments (RowPipe), for rows of 32 or 64 segments
 // whose slots are in device memory.
 template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false, int NP = 1>
