@@ -210,9 +210,14 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out);
  * which hides a launch's start-up latency behind the previous launch's tail.
  * Every write (output rows, status word) still waits for that kernel to
  * complete, so a kernel that reads the previous call's output is unaffected.
- * If the kernel just before does write the call's inputs, the call may read
- * stale values: leave the hint off then (a copy or an event between the two
- * is not a kernel and keeps full ordering).  Used by ibp_gather_decompress,
+ * This library's decompress and status-read kernels let the kernel after them
+ * start early in the same way, so when the kernel just before is one of them,
+ * the inputs must not be written by the kernels before it either, back to
+ * the first kernel that is not one of them (e.g. decompress, status read,
+ * decompress: the second decompress must not read what the first one
+ * writes).  If those kernels do write the call's inputs, the call may read
+ * stale values: leave the hint off then (a copy or an event between them is
+ * not a kernel and keeps full ordering).  Used by ibp_gather_decompress,
  * ibp_decompress_contig, ibp_gather_decompress_packed,
  * ibp_gather_decompress_bag and ibp_decompress_contig_set (each plan's hints
  * as the set copied them).
