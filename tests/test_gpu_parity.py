@@ -551,3 +551,49 @@ def test_ids_and_status_word_in_pinned_host_memory(where):
     dword = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     ibp.ibp_get_status_async(g["plan"], dword[0])
     assert int(dword.item()) == ibp.IBP_OK
+
+
+@pytest.mark.parametrize("W", [64, 128, 512])
+@pytest.mark.parametrize("where", ["host", "hbm"])
+def test_per_word_plan_groups_with_raw_corrupt_and_bad_rows(W, where):
+    """Per-word tables (two Masks alternating by word position; one run of
+    kept bits each) on groups that mix compressed, raw and corrupt rows and
+    bad ids: from device slots the rows are rebuilt two words per lane, with
+    straight-line code for groups whose rows are all compressed and a per-row
+    path for the others.  Rows and status against the oracle's decode of the
+    same slots."""
+    rng = np.random.default_rng(40 + W)
+    n = 600
+    rows = _float_rows(rng, n, W)
+    mask = np.where(np.arange(W) % 2 == 0, 0xFF800000, 0xFFF00000).astype(np.uint32)
+    bitval = (rows[0] & mask).astype(np.uint32)
+    match = rng.random((n, 1)) < 0.8
+    rows = np.where(match, (rows & ~mask) | (bitval & mask), rows).astype(np.uint32)
+    plan = _explicit_plan_check(mask, bitval, rows, where)
+    assert plan.info["uniform"] == 0 and plan.info["max_runs"] == 1
+    rows_t = place(rows, where)
+    slots_t = empty_like_in(rows_t, where)
+    _, bm, _ = ibp.ibp_compress(plan, rows_t, slots_t)
+    torch.cuda.synchronize()
+    bitmask = words_np(bm)
+    slots = words_np(slots_t).copy()
+    comp = np.nonzero((bitmask[np.arange(n) >> 5] >> (np.arange(n) & 31).astype(np.uint32)) & 1)[0]
+    raw_rows = np.setdiff1d(np.arange(n), comp)
+    assert len(comp) > 50 and len(raw_rows) > 5
+    bad_rows = comp[3:9]
+    slots[bad_rows, :W // 32] = 0  # every word announced raw: stream >= W words
+    dev = place(slots, where)
+    ids = rng.integers(0, n, 3000).astype(np.int64)
+    ids[::37] = bad_rows[np.arange(len(ids[::37])) % len(bad_rows)]
+    ids[5::101] = n + 3
+    out = ibp.ibp_gather_decompress(plan, dev, bm, torch.from_numpy(ids).cuda())
+    code = ibp.ibp_get_status(plan, raise_on_error=False)
+    st, ref = C.decompress(slots, bitmask, ids, mask, bitval)
+    assert code in (ibp.IBP_ERANGE, ibp.IBP_ECORRUPT) and st in (ibp.IBP_ERANGE, ibp.IBP_ECORRUPT)
+    assert np.array_equal(words_np(out), ref)
+    # all-compressed groups only: the straight-line path, status clean
+    good = np.setdiff1d(comp, bad_rows)
+    ids = good[rng.integers(0, len(good), 2000)].astype(np.int64)
+    out = ibp.ibp_gather_decompress(plan, dev, bm, torch.from_numpy(ids).cuda())
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+    assert np.array_equal(words_np(out), rows[ids])
