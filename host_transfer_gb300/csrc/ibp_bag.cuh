@@ -20,8 +20,9 @@
 // cursor cuts each bag into groups of at most G consecutive ids (a group
 // never spans two bags; an empty or invalid bag is one group of no rows), and
 // the decode of a group adds its rows, in order, into the lanes'
-// accumulators (word lane + 32 s in acc[s]); the group that ends a bag
-// writes the bag's output row.
+// accumulators (word lane + 32 s in acc[s]; under per-word tables, when a
+// warp pools whole rows, word 64 k + 2 lane + i in acc[2 k + i]); the group
+// that ends a bag writes the bag's output row.
 #pragma once
 
 #include "ibp_decompress_fast.cuh"

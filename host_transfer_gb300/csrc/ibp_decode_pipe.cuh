@@ -18,8 +18,10 @@
 //                 bad id, corrupt), its stream length Lw, and where each
 //                 segment's fields start in its row's stream;
 //   issue_rest    the words [pre, Lw) of each row (W for raw rows);
-// and then, per row, decode_row / decode_segments with a caller-supplied
-// sink that stores the rebuilt words (gather) or adds them up (pooling).
+// and then, per row, decode_row / decode_segments (one word per lane and
+// segment) or, with PAIR, decode_row_pairs / decode_pairs_at (two
+// consecutive words per lane and 64-word block), with a caller-supplied sink
+// that stores the rebuilt words (gather) or adds them up (pooling).
 //
 // Shapes are compile-time: W = 32 * SC words per row, at most R runs of kept
 // bits per word, uniform plan (TAB = false: one Mask/Bitval for every word
