@@ -256,6 +256,7 @@ int ibp_plan_get_info(const ibp_plan* plan, ibp_plan_info* out) {
   out->metadata_bytes = plan->d_bytes;
   out->device = plan->device;
   out->prefix_words = prefix_words(plan, true);
+  out->short_rows = plan->short_rows;
   return IBP_OK;
 }
 
@@ -325,6 +326,15 @@ int ibp_plan_tune_prefix(ibp_plan* plan, const uint32_t* slots, uint64_t n_rows,
     }
   }
   plan->prefix = static_cast<uint32_t>(4ull * best_p < W ? 4ull * best_p : W);
+  // Short rows: at least 99 % of the sampled rows store at most W / 4 words
+  // (raw rows store W).  Decodes from device memory then stage W / 4 words
+  // per row and read the few longer rows from their slots.
+  uint64_t total = 0, short_n = 0;
+  for (uint32_t c = 0; c < nb; ++c) {
+    total += hist[c];
+    if (4ull * c <= W / 4) short_n += hist[c];
+  }
+  plan->short_rows = (total > 0 && 100ull * short_n >= 99ull * total) ? 1u : 0u;
   if (prefix_words_out) *prefix_words_out = prefix_words(plan, W % 4 == 0);
   return IBP_OK;
 }

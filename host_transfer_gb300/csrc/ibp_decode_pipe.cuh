@@ -59,11 +59,16 @@ struct TabShape {
 // that its segments' fields occupy (at most W / NP words plus alignment), so
 // stages stay smaller than a row's and more warps fit on an SM; each task
 // re-reads the row's headers.
-template <int SC, uint32_t GW, int NP = 1>
+// SHORT (rows of 8 or 16 segments whose stored streams are mostly at most
+// W / 4 words, slots in device memory): a stage row holds RW = W / 4 words,
+// so stages are a quarter of the size; a row whose stream is longer is
+// decoded from its slot in device memory, and a raw row is copied from it.
+template <int SC, uint32_t GW, int NP = 1, bool SHORT = false>
 struct FastShape {
   static constexpr uint32_t W = 32u * SC;
+  static constexpr uint32_t RW = SHORT ? W / 4u : W;  // words per stage row
   static constexpr uint32_t G = NP > 1 ? 1u : (GW / W >= 1 ? GW / W : 1u);  // rows (tasks) per group
-  static constexpr uint32_t STAGE = NP > 1 ? SC + W / NP + 32u : G * W + 32u;  // words per stage
+  static constexpr uint32_t STAGE = NP > 1 ? SC + W / NP + 32u : G * RW + 32u;  // words per stage
   static constexpr uint32_t CH = W / 4;                    // 16-byte chunks per row
   static constexpr uint32_t CB = (CH + 31) / 32;           // chunk blocks of 32 per row
 };
@@ -83,17 +88,19 @@ struct RowPos {
 // each lane two consecutive words of every 64-word block (decode_pairs_at),
 // written with one 8-byte store per lane; the per-word tables are then staged
 // in the order the lanes read them (see init).
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, int NP = 1, bool PAIR = false>
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, int NP = 1, bool PAIR = false,
+          bool SHORT = false>
 struct RowPipe {
-  using F = FastShape<SC, GW, NP>;
+  using F = FastShape<SC, GW, NP, SHORT>;
   using T = TabShape<SC, R, NPL, TAB>;
-  static constexpr uint32_t W = F::W, G = F::G, CB = F::CB;
+  static constexpr uint32_t W = F::W, G = F::G, CB = F::CB, RW = F::RW;
   static constexpr uint32_t EW = TabEntry<R>::EW;
   static constexpr uint32_t PCB = NP > 1 ? (SC / 4 + 31) / 32 : CB;  // chunk blocks a prefix can span
   static constexpr uint32_t SEGP = SC / NP;  // segments of a task
   static constexpr uint32_t WP = W / NP;     // output words of a task
   static_assert(NP == 1 || (!PK && SC >= 32 && (SEGP == 16 || SEGP == 32)), "tasks of 16 or 32 segments, slot layout");
   static_assert(!PAIR || SC >= 2, "pairs need 64-word blocks");
+  static_assert(!SHORT || (PAIR && !PK && NP == 1 && SC >= 8), "short stage rows: pair decode, slots, whole rows");
 
   uint32_t lane, lt, lanebit;
   uint32_t half, j0, plt, pbit0, pbit1;  // PAIR: segment 2k + half, positions j0, j0 + 1
@@ -192,7 +199,7 @@ struct RowPipe {
       if constexpr (PK) ok = ok && __shfl_sync(kAll, rp.ext, q) >= pre;
       if (ok) {
         const uint32_t* src = slots + offq;
-        uint32_t* dst = sb + q * W;
+        uint32_t* dst = sb + q * RW;
         // blocks of 32 chunks up to the prefix's last (a task's prefix, its
         // row's headers, is at most one block)
 #pragma unroll
@@ -242,7 +249,7 @@ struct RowPipe {
     auto bits_of = [&](uint32_t f) -> uint32_t {
       if (f >= NSEG) return 0u;
       const uint32_t q = f / SC, s = f % SC;
-      return seg_bits(sb[q * W + s], s);
+      return seg_bits(sb[q * RW + s], s);
     };
     auto scan = [&](uint32_t v) -> uint32_t {  // inclusive, within groups of SW lanes
 #pragma unroll
@@ -307,7 +314,7 @@ struct RowPipe {
       if constexpr (NP > 1)
         nt = ((part * (WP / 4u)) << 16) | ((part + 1u) * (WP / 4u));
       else
-        nt = kind == kRaw ? W : 0u;
+        nt = (kind == kRaw && !SHORT) ? W : 0u;  // SHORT: a raw row is copied from its slot
       return;
     }
     if (PK && rp.ext < pre) {
@@ -327,6 +334,7 @@ struct RowPipe {
       nt = ((ws >> 2) << 16) | ((we + 3u) >> 2);
     } else {
       nt = Lw;
+      if (SHORT && Lw > RW) kind = kCompSlot;  // decoded from its slot
     }
   }
 
@@ -354,7 +362,7 @@ struct RowPipe {
       else
         offq = static_cast<uint64_t>(__shfl_sync(kAll, id, q)) * W;
       const uint32_t* src = slots + offq;
-      uint32_t* dst = sb + q * W;
+      uint32_t* dst = sb + q * RW;
       for (uint32_t c = pre_ch + lane; c < ((ntq + 3u) >> 2); c += 32) cp_row16(reuse, dst + 4u * c, src + 4u * c);
     }
   }
@@ -493,6 +501,14 @@ struct RowPipe {
   __device__ __forceinline__ void decode_row_pairs(const uint32_t* pb, uint32_t q, const Bases& bases,
                                                    Sink&& sink) const {
     decode_pairs_at<SC>(pb, pb, 0u, [&](uint32_t j) { return seg_base_pair(bases, q, j); }, sink);
+  }
+
+  // As decode_row_pairs, with the row's headers at hb and its stream at pb
+  // (SHORT: a row too long for its stage row, read from its slot).
+  template <class Sink>
+  __device__ __forceinline__ void decode_row_pairs_from(const uint32_t* hb, const uint32_t* pb, uint32_t q,
+                                                        const Bases& bases, Sink&& sink) const {
+    decode_pairs_at<SC>(hb, pb, 0u, [&](uint32_t j) { return seg_base_pair(bases, q, j); }, sink);
   }
 
   // PAIR: the base of segment j of row q where j = 2k + half differs between

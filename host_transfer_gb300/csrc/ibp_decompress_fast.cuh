@@ -68,6 +68,15 @@ constexpr bool kPairTable = true;
 // (80 -> 135) and so fewer CTAs (per-head K/V plan sets from host slots
 // 227 -> 174 GB/s).
 constexpr bool kStraightTable = true;
+// Rows whose stored streams are mostly short (at most W / 4 words, as
+// ibp_plan_tune_prefix records) take stage rows of W / 4 words when their
+// slots are in device memory (per-word tables of up to two runs and one
+// e-plane, rows of 256 or 512 words): the stages shrink to a quarter, so the
+// register budget (80, three CTAs of eight warps) rather than shared memory
+// bounds the warps per SM, and the rare longer rows are decoded from their
+// slots.  Sparse rows from HBM 3476 -> 3775 GB/s (0.62 -> 0.67 of the HBM
+// peak); a four-CTA budget (64 registers) measured 0.55.
+constexpr bool kShortRows = true;
 
 // PK = false: row r of the table is slots[r * W ..]; PK = true: the packed
 // layout, row r is slots[offsets[r] .. offsets[r + 1]) (its stored words
@@ -88,9 +97,11 @@ constexpr bool kStraightTable = true;
 // Rows split into tasks (NP > 1): a register budget for three CTAs (tasks of
 // 32 segments, whose stages leave two CTAs per SM, measured the same with a
 // budget for two).
-template <int SC, int NPL, bool TAB, bool MP, bool DEV, uint32_t GW, int NP = 1>
+// Short stage rows (SHORT) leave room for four CTAs or more; a budget for
+// three measured best (see kShortRows).
+template <int SC, int NPL, bool TAB, bool MP, bool DEV, uint32_t GW, int NP = 1, bool SHORT = false>
 constexpr int fast_min_blocks() {
-  if (NP > 1) return 3;
+  if (NP > 1 || SHORT) return 3;
   if (!TAB) return DEV ? (SC <= 32 ? 3 : 1) : (SC <= 32 ? 4 : 1);
   if (DEV && !MP && SC <= 16 && NPL <= 1) return GW >= 1024 ? 2 : 3;
   return 1;
@@ -101,15 +112,17 @@ constexpr int fast_min_blocks() {
 // straight-line groups.  NP > 1: every row
 // is NP tasks of SC / NP segments (RowPipe), for rows of 32 or 64 segments
 // whose slots are in device memory.
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false, int NP = 1>
-__global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV, GW, NP>())) k_decompress_fast(const DecodeArgs a) {
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false, int NP = 1,
+          bool SHORT = false>
+__global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB, MP, DEV, GW, NP, SHORT>()))
+    k_decompress_fast(const DecodeArgs a) {
   static_assert(!MP || (TAB && !PK), "plan sets decode through the table path, slot layout");
   static_assert(NP == 1 || !MP, "plan sets decode whole rows");
   constexpr bool PAIR = SC >= 2 && (TAB ? kPairTable && DEV : kPairUniform);
-  using Pipe = RowPipe<R, SC, NPL, TAB, PK, GW, NP, PAIR>;
+  using Pipe = RowPipe<R, SC, NPL, TAB, PK, GW, NP, PAIR, SHORT>;
   using F = typename Pipe::F;
   using T = typename Pipe::T;
-  constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB;
+  constexpr uint32_t W = F::W, G = F::G, STAGE = F::STAGE, CB = F::CB, RW = F::RW;
   extern __shared__ __align__(128) uint32_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
@@ -193,7 +206,9 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
       reinterpret_cast<uint4*>(orow)[c] = k0 == kRaw ? prow[c] : make_uint4(0, 0, 0, 0);
   };
 
-  auto decode_group = [&](const uint32_t* sb, uint64_t rbase, uint32_t kind, const typename Pipe::Bases& bases) {
+  // id: lane q < G holds row q's id (SHORT: rows read from their slots).
+  auto decode_group = [&](const uint32_t* sb, uint64_t rbase, uint32_t kind, const typename Pipe::Bases& bases,
+                          int32_t id) {
     uint32_t* const obase = out + rbase * W + lane;
     const uint32_t comp = __ballot_sync(kAll, kind == kComp);
     const uint32_t raw = __ballot_sync(kAll, kind == kRaw);
@@ -205,7 +220,7 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     auto decode_comp = [&](uint32_t q) {
       if constexpr (PAIR) {
         uint2* const o2 = reinterpret_cast<uint2*>(obase - lane + q * W) + lane;
-        pp.decode_row_pairs(sb + q * W, q, bases,
+        pp.decode_row_pairs(sb + q * RW, q, bases,
                             [&](uint32_t k, uint32_t y0, uint32_t y1) { o2[32u * k] = make_uint2(y0, y1); });
       } else {
         uint32_t* o = obase + q * W;
@@ -222,6 +237,33 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
       for (uint32_t q = 0; q < G; ++q) {
         if ((comp >> q) & 1u) decode_comp(q);
       }
+    }
+    if constexpr (SHORT) {
+      // rows that have no stage row: compressed rows longer than RW words,
+      // decoded from their slots (headers from the stage), and raw rows,
+      // copied from their slots in 16-byte chunks; then bad ids and corrupt
+      // rows, zero-filled
+      const uint32_t slotm = __ballot_sync(kAll, kind == kCompSlot);
+      for (uint32_t m = slotm | raw | badm; m; m &= m - 1) {
+        const uint32_t q = __ffs(m) - 1;
+        const int32_t idq = __shfl_sync(kAll, id, q);
+        uint32_t* const orow = obase - lane + q * W;
+        if ((slotm >> q) & 1u) {
+          uint2* const o2 = reinterpret_cast<uint2*>(orow) + lane;
+          pp.decode_row_pairs_from(sb + q * RW, a.slots + static_cast<uint64_t>(idq) * W, q, bases,
+                                   [&](uint32_t k, uint32_t y0, uint32_t y1) { o2[32u * k] = make_uint2(y0, y1); });
+        } else {
+          const bool r = (raw >> q) & 1u;
+          const uint4* const prow = reinterpret_cast<const uint4*>(a.slots + static_cast<uint64_t>(r ? idq : 0) * W);
+#pragma unroll
+          for (uint32_t b = 0; b < CB; ++b) {
+            const uint32_t c = lane + 32u * b;
+            if (c < F::CH) reinterpret_cast<uint4*>(orow)[c] = r ? prow[c] : make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      if (bad) record_status(pv.status, kind == kBadRange ? IBP_ERANGE : IBP_ECORRUPT);
+      return;
     }
     if (raw == kGroupBits) {
       // every row raw (e.g. K/V rows of 64 words that no Mask compresses): the
@@ -306,7 +348,7 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
     if constexpr (NP > 1)
       decode_task(st[0], rb0, kind0, nt0, bases0);
     else
-      decode_group(st[0], rb0, kind0, bases0);
+      decode_group(st[0], rb0, kind0, bases0, idr[0]);
     __syncwarp();
     kind0 = kind1;
     nt0 = nt1;
@@ -327,9 +369,10 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
   cp_wait<0>();
 }
 
-template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false, int NP = 1>
+template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = false, bool DEV = false, int NP = 1,
+          bool SHORT = false>
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
-  using F = FastShape<SC, GW, NP>;
+  using F = FastShape<SC, GW, NP, SHORT>;
   using T = TabShape<SC, R, NPL, TAB>;
   const size_t per_warp = 4ull * kFastStages * F::STAGE;
   const size_t fixed = 4ull * T::WORDS;
@@ -337,7 +380,7 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
   if (warps < 1) return IBP_EINVAL;
   const size_t smem = fixed + warps * per_warp;
-  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW, MP, DEV, NP>;
+  auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW, MP, DEV, NP, SHORT>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
   // for this launch shape.
   static int occ_cache[64] = {0};
@@ -424,8 +467,31 @@ static int launch_table_r(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stre
   }
 }
 
+// Short stage rows (slots in device memory, per-word tables, rows of 8 or 16
+// segments, at most one e-plane), two rows per group: with four (256-word
+// rows in 1024-word groups) the straight-line group spilled registers.
+template <int R>
+static int launch_fast_short(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  const bool e0 = plan->view.npl == 0;
+  if (plan->S == 8)
+    return e0 ? launch_fast_t<R, 8, 0, true, false, 512, false, true, 1, true>(plan, a, stream)
+              : launch_fast_t<R, 8, 1, true, false, 512, false, true, 1, true>(plan, a, stream);
+  return e0 ? launch_fast_t<R, 16, 0, true, false, 1024, false, true, 1, true>(plan, a, stream)
+            : launch_fast_t<R, 16, 1, true, false, 1024, false, true, 1, true>(plan, a, stream);
+}
+
 template <bool PK, uint32_t GW, bool DEV = false>
 static int launch_fast_table_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
+  // rows of 8 or 16 segments in device memory whose stored streams are
+  // mostly at most W / 4 words (ibp_plan_tune_prefix found so), at most two
+  // runs of kept bits per word, at most one e-plane: stage rows of W / 4 words
+  if constexpr (DEV && !PK && kShortRows) {
+    if (plan->short_rows && plan->max_runs <= 2 && plan->view.npl <= 1 && a.pre <= plan->W / 4u &&
+        (plan->S == 8 || plan->S == 16)) {
+      if (plan->max_runs <= 1) return launch_fast_short<1>(plan, a, stream);
+      return launch_fast_short<2>(plan, a, stream);
+    }
+  }
   // one run of kept bits per word and at most one e-plane (the sparse tables'
   // plans): a one-run deposit per word instead of two
   if (plan->max_runs <= 1 && plan->view.npl <= 1)

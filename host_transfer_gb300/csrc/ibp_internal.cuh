@@ -18,8 +18,9 @@ constexpr int kMaxRuns = 4;     // runs of kept bits handled by the run tables
 constexpr int kPlanes = 6;      // bit planes of a kept-bit count (0..32)
 constexpr int kWarp = 32;
 
-// Row kinds decided before a row's payload is fetched.
-enum RowKind : uint32_t { kNone = 0, kRaw = 1, kComp = 2, kBadRange = 3, kCorrupt = 4 };
+// Row kinds decided before a row's payload is fetched (kCompSlot: a
+// compressed row decoded from its slot instead of a shared-memory stage).
+enum RowKind : uint32_t { kNone = 0, kRaw = 1, kComp = 2, kBadRange = 3, kCorrupt = 4, kCompSlot = 5 };
 
 // Device view of a plan, passed to kernels by value.
 //
@@ -73,6 +74,7 @@ struct ibp_plan {
   uint32_t uniform, max_runs, min_kept, max_kept;
   uint32_t lmin;  // min(W, words of the shortest possible compressed stream)
   uint32_t prefix;  // words fetched before the headers (slot layout); 0 = from lmin
+  uint32_t short_rows;  // the tuner found 99 % of the sampled rows at most W / 4 words long
   void* d_block;  // single device allocation holding every table + status
   uint32_t* h_status;  // pinned host word the status is read back into
   std::mutex status_mu;  // serialises ibp_get_status calls on this plan (h_status)

@@ -57,7 +57,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("W", ctypes.c_uint32), ("segments", ctypes.c_uint32), ("uniform", ctypes.c_uint32),
                 ("max_runs", ctypes.c_uint32), ("min_kept_bits", ctypes.c_uint32),
                 ("max_kept_bits", ctypes.c_uint32), ("metadata_bytes", ctypes.c_uint64),
-                ("device", ctypes.c_int), ("prefix_words", ctypes.c_uint32)]
+                ("device", ctypes.c_int), ("prefix_words", ctypes.c_uint32),
+                ("short_rows", ctypes.c_uint32)]
 
 
 def load():

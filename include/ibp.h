@@ -99,6 +99,10 @@ typedef struct ibp_plan_info {
   int device;              /* CUDA device of the plan */
   uint32_t prefix_words;   /* words a decompress call fetches from every slot before
                               reading the row's headers (slot layout, aligned buffers) */
+  uint32_t short_rows;     /* 1 when ibp_plan_tune_prefix found at least 99 % of the
+                              sampled rows storing at most W / 4 words: decodes of
+                              per-word-table plans from device memory then stage W / 4
+                              words per row and read longer rows from their slots */
 } ibp_plan_info;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -244,7 +248,13 @@ int ibp_plan_set_hints(ibp_plan* plan, uint32_t hints);
  * sets the prefix P (in chunks, from the default up to W) that minimises
  * sum over sampled rows of (c > P ? c + 8 : P), c the row's chunks: words
  * fetched plus a penalty of 8 chunks for each second fetch.  The prefix in
- * words is written to *prefix_words when that is not NULL.  slots and bitmask
+ * words is written to *prefix_words when that is not NULL.  From the same
+ * sample it records whether at least 99 % of the rows store at most W / 4
+ * words (ibp_plan_info.short_rows): then decodes of per-word-table plans with
+ * rows of 256 or 512 words (at most two runs of kept bits per word and two
+ * kept-bit counts) from device memory stage W / 4 words per row, so
+ * more warps fit on an SM, and read the few longer rows from their slots
+ * (when the prefix is at most W / 4 words).  slots and bitmask
  * are as for ibp_gather_decompress (host-mapped or device memory).
  * Synchronises `stream`.  Errors: IBP_EINVAL, IBP_ENOMEM, IBP_ECUDA.
  *

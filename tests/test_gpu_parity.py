@@ -597,3 +597,53 @@ def test_per_word_plan_groups_with_raw_corrupt_and_bad_rows(W, where):
     out = ibp.ibp_gather_decompress(plan, dev, bm, torch.from_numpy(ids).cuda())
     assert ibp.ibp_get_status(plan) == ibp.IBP_OK
     assert np.array_equal(words_np(out), rows[ids])
+
+
+@pytest.mark.parametrize("W", [256, 512])
+def test_short_stage_rows_from_device_slots(W):
+    """Sparse rows (5 % non-zeros) under a per-word plan, slots in HBM: once
+    the prefix is tuned the plan records short rows and device decodes stage
+    W / 4 words per row.  A few denser rows (stored longer than W / 4 words,
+    decoded from their slots), raw rows (copied from their slots), corrupt
+    rows and bad ids mixed in; rows and status against the oracle's decode of
+    the same slots."""
+    rng = np.random.default_rng(70 + W)
+    n = 6000
+    rows = workloads.sparse_gnn_table(n_rows=n, W=W, seed=W, nnz=max(1, W // 20))
+    dense = rng.choice(n, 20, replace=False)  # 0.33 %: long compressed rows
+    raw = rng.choice(np.setdiff1d(np.arange(n), dense), 12, replace=False)  # 0.2 %: raw rows
+    rows[dense, : 2 * W // 5] = rng.lognormal(-2, 0.5, (len(dense), 2 * W // 5)).astype(np.float32).view(np.uint32)
+    rows[raw] = rng.integers(0, 2**32, (len(raw), W), dtype=np.uint64).astype(np.uint32)
+    g = gpu_codec(rows, rows[:3000], 0.95, "hbm")
+    plan = g["plan"]
+    assert plan.info["uniform"] == 0 and plan.info["max_runs"] <= 2
+    bm = on_device(g["bitmask"])
+    words = ibp.ibp_plan_tune_prefix(plan, g["slots_t"], bm)
+    info = plan.info
+    assert info["short_rows"] == 1 and words <= W // 4
+    slots = words_np(g["slots_t"]).copy()
+    comp = np.nonzero((g["bitmask"][np.arange(n) >> 5] >> (np.arange(n) & 31).astype(np.uint32)) & 1)[0]
+    assert np.isin(dense, comp).all() and not np.isin(raw, comp).any()
+    bad = np.setdiff1d(comp, dense)[:4]
+    slots[bad, : W // 32] = 0  # every word announced raw: stream >= W words
+    dev = on_device(slots)
+    ids = rng.integers(0, n, 20000).astype(np.int64)
+    ids[::50] = dense[np.arange(len(ids[::50])) % len(dense)]
+    ids[7::80] = raw[np.arange(len(ids[7::80])) % len(raw)]
+    ids[11::997] = bad[np.arange(len(ids[11::997])) % len(bad)]
+    ids[13::1999] = -5
+    out = ibp.ibp_gather_decompress(plan, dev, bm, torch.from_numpy(ids).cuda())
+    code = ibp.ibp_get_status(plan, raise_on_error=False)
+    st, ref = C.decompress(slots, g["bitmask"], ids, g["mask"], g["bitval"])
+    assert code in (ibp.IBP_ERANGE, ibp.IBP_ECORRUPT) and st in (ibp.IBP_ERANGE, ibp.IBP_ECORRUPT)
+    assert np.array_equal(words_np(out), ref)
+    # clean ids only: every row exact, status clean; contiguous too
+    ok = np.setdiff1d(np.arange(n), bad)
+    ids = ok[rng.integers(0, len(ok), 20000)].astype(np.int64)
+    out = ibp.ibp_gather_decompress(plan, dev, bm, torch.from_numpy(ids).cuda())
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+    assert np.array_equal(words_np(out), rows[ids])
+    first = int(bad.max()) + 1
+    out = ibp.ibp_decompress_contig(plan, dev, bm, first, n - first)
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+    assert np.array_equal(words_np(out), rows[first:])
