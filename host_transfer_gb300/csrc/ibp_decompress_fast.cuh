@@ -75,8 +75,12 @@ constexpr bool kStraightTable = true;
 // register budget (80, three CTAs of eight warps) rather than shared memory
 // bounds the warps per SM, and the rare longer rows are decoded from their
 // slots.  Sparse rows from HBM 3476 -> 3775 GB/s (0.62 -> 0.67 of the HBM
-// peak); a four-CTA budget (64 registers) measured 0.55.
+// peak); a four-CTA budget (64 registers) measured 0.55.  The small stages
+// also make room for a deeper pipeline: four stages 0.67 -> 0.68 (five 0.64,
+// six 0.61: the extra stages' state costs registers); a prefix of RW words,
+// so that no row of at most RW words needs a second fetch, measured 0.66.
 constexpr bool kShortRows = true;
+constexpr int kShortStages = 4;  // shared-memory stages per warp with short stage rows
 
 // PK = false: row r of the table is slots[r * W ..]; PK = true: the packed
 // layout, row r is slots[offsets[r] .. offsets[r + 1]) (its stored words
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(kFastWarps * 32, (fast_min_blocks<SC, NPL, TAB
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t nw_cta = blockDim.x >> 5;
-  constexpr int D = kFastStages;
+  constexpr int D = SHORT ? kShortStages : kFastStages;
   uint32_t* const stages = smem + T::WORDS + warp * static_cast<uint32_t>(D) * STAGE;
 
   // this CTA's plan, row range and output
@@ -374,7 +378,7 @@ template <int R, int SC, int NPL, bool TAB, bool PK, uint32_t GW, bool MP = fals
 static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t stream) {
   using F = FastShape<SC, GW, NP, SHORT>;
   using T = TabShape<SC, R, NPL, TAB>;
-  const size_t per_warp = 4ull * kFastStages * F::STAGE;
+  const size_t per_warp = 4ull * (SHORT ? kShortStages : kFastStages) * F::STAGE;
   const size_t fixed = 4ull * T::WORDS;
   size_t warps = (220ull * 1024 - fixed) / per_warp;
   if (warps > static_cast<size_t>(kFastWarps)) warps = kFastWarps;
