@@ -78,7 +78,8 @@ constexpr bool kStraightTable = true;
 // peak); a four-CTA budget (64 registers) measured 0.55.  The small stages
 // also make room for a deeper pipeline: four stages 0.67 -> 0.68 (five 0.64,
 // six 0.61: the extra stages' state costs registers); a prefix of RW words,
-// so that no row of at most RW words needs a second fetch, measured 0.66.
+// so that no row of at most RW words needs a second fetch, measured 0.66;
+// seven or six warps per CTA (97 or 113 registers) 0.61 and 0.60.
 constexpr bool kShortRows = true;
 constexpr int kShortStages = 4;  // shared-memory stages per warp with short stage rows
 
