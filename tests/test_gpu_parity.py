@@ -647,3 +647,48 @@ def test_short_stage_rows_from_device_slots(W):
     out = ibp.ibp_decompress_contig(plan, dev, bm, first, n - first)
     assert ibp.ibp_get_status(plan) == ibp.IBP_OK
     assert np.array_equal(words_np(out), rows[first:])
+
+
+@pytest.mark.parametrize("W", [256, 512])
+def test_short_stage_rows_at_the_stage_boundary(W):
+    """Short stage rows hold W / 4 words: rows whose streams are W / 4 - 1,
+    W / 4 (staged) and W / 4 + 1, W / 4 + 2 words (decoded from their slots),
+    among rows that all fit, under an explicit per-word plan (one and two
+    kept bits, alternating).  Stored lengths come from the oracle."""
+    rng = np.random.default_rng(500 + W)
+    RW = W // 4
+    mask = np.where(np.arange(W) % 2 == 0, 0xFFFFFFFE, 0xFFFFFFFC).astype(np.uint32)
+    bitval = np.zeros(W, np.uint32)
+    base = rng.integers(0, 2, (1, W)).astype(np.uint32)  # every word matches
+
+    def with_unmatched(k):
+        r = base.copy()
+        pos = rng.choice(W, k, replace=False)
+        r[0, pos] = rng.integers(1 << 20, 1 << 31, k).astype(np.uint32)
+        return r
+
+    # candidates around the boundary: the oracle's stored length picks them
+    cands = np.concatenate([with_unmatched(k) for k in range(1, W // 2) for _ in range(3)])
+    lw = C.row_words(cands, mask, bitval)
+    picks = [cands[lw == L][:3] for L in (RW - 1, RW, RW + 1, RW + 2)]
+    assert all(len(p) for p in picks), [int((lw == L).sum()) for L in (RW - 1, RW, RW + 1, RW + 2)]
+    n = 4000
+    rows = np.repeat(base, n, axis=0)
+    rows ^= (rng.random((n, W)) < 0.5).astype(np.uint32)  # kept bits only: still matching
+    special = np.concatenate(picks)
+    at = rng.choice(n, len(special), replace=False)
+    rows[at] = special
+    plan = ibp.ibp_plan_create(torch.from_numpy(mask.view(np.int32)), torch.from_numpy(bitval.view(np.int32)))
+    rows_t = on_device(rows)
+    slots_t = torch.empty_like(rows_t)
+    _, bm, _ = ibp.ibp_compress(plan, rows_t, slots_t)
+    ibp.ibp_plan_tune_prefix(plan, slots_t, bm)
+    assert plan.info["short_rows"] == 1 and plan.info["prefix_words"] <= RW
+    slots = words_np(slots_t)
+    cs, cb, _ = C.compress(rows, mask, bitval)
+    assert np.array_equal(slots, cs) and np.array_equal(words_np(bm), cb)
+    ids = np.concatenate([np.repeat(at, 5), rng.integers(0, n, 6000)]).astype(np.int64)
+    rng.shuffle(ids)
+    out = ibp.ibp_gather_decompress(plan, slots_t, bm, torch.from_numpy(ids).cuda())
+    assert ibp.ibp_get_status(plan) == ibp.IBP_OK
+    assert np.array_equal(words_np(out), rows[ids])
