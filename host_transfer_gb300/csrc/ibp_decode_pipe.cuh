@@ -37,11 +37,6 @@
 namespace ibp {
 
 constexpr uint32_t kAll = 0xFFFFFFFFu;
-// Prefixes of at most 16 chunks (64-word rows: DLRM, the LLM's K and V) are
-// copied two rows per warp step, a half-warp per row, instead of one row per
-// step with half the lanes idle (LLM layer step from HBM 0.94 -> 0.97 of the
-// HBM peak; DLRM unchanged).
-constexpr bool kPairedPrefix = true;
 
 // Words of a per-word table entry in shared memory: {run masks, packed run
 // shifts, Bitval & Mask}: 4 words for up to two runs, 8 for up to four.
@@ -190,21 +185,6 @@ struct RowPipe {
   // chunk i (+32 ...) of every row's first `pre` words.  Warp-collective.
   __device__ __forceinline__ void issue_prefix(uint32_t* sb, int32_t id, RowPos rp, uint32_t& bmw) const {
     if (id >= 0) bmw = ld_u32(bitmask + (static_cast<uint32_t>(id) >> 5));
-    if constexpr (!PK && NP == 1 && G >= 2 && kPairedPrefix) {
-      // prefixes of at most 16 chunks (64-word rows): each half-warp copies
-      // one row, two rows per step
-      if (pre_ch <= 16u) {
-        const uint32_t c = lane & 15u;
-#pragma unroll
-        for (uint32_t q2 = 0; q2 < G; q2 += 2) {
-          const uint32_t q = q2 + (lane >> 4);
-          const int32_t idq = __shfl_sync(kAll, id, q < G ? q : 0u);
-          if (q < G && idq >= 0 && c < pre_ch)
-            cp_row16(reuse, sb + q * RW + 4u * c, slots + static_cast<uint64_t>(idq) * W + 4u * c);
-        }
-        return;
-      }
-    }
 #pragma unroll
     for (uint32_t q = 0; q < G; ++q) {
       const int32_t idq = __shfl_sync(kAll, id, q);
