@@ -64,14 +64,18 @@ int resolve_ptr(const void* p, int device, const void** dev) {
 }
 
 int sm_count(int device) {
-  static int cached[64] = {0};
-  if (device >= 0 && device < 64 && cached[device]) return cached[device];
+  // per device; set once, read by any host thread
+  static std::atomic<int> cached[64];
+  if (device >= 0 && device < 64) {
+    const int c = cached[device].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = 1;
   }
-  if (device >= 0 && device < 64) cached[device] = n;
+  if (device >= 0 && device < 64) cached[device].store(n, std::memory_order_relaxed);
   return n;
 }
 

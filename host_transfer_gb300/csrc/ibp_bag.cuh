@@ -271,10 +271,10 @@ static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
   const size_t smem = fixed + warps * per_warp;
   if (warps % CS != 0) return IBP_EINVAL;  // a team's warps share a CTA
   auto kern = k_bag<R, SC, NPL, TAB, GW, BF16, CS>;
-  static int occ_cache[64] = {0};
+  static std::atomic<int> occ_cache[64];  // per device, any host thread
   const int dev = plan->device;
   if (dev < 0 || dev >= 64) return IBP_EINVAL;
-  int occ = occ_cache[dev];
+  int occ = occ_cache[dev].load(std::memory_order_relaxed);
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
@@ -284,7 +284,7 @@ static int launch_bag_t(const ibp_plan* plan, BagArgs& a, cudaStream_t stream) {
       cudaGetLastError();
       return IBP_ECUDA;
     }
-    occ_cache[dev] = occ;
+    occ_cache[dev].store(occ, std::memory_order_relaxed);
   }
   const uint64_t need = (a.n_bags * CS + warps - 1) / warps;
   const uint64_t cap = static_cast<uint64_t>(occ) * sm_count(dev);

@@ -189,11 +189,11 @@ static int launch_t(const ibp_plan* plan, CompressArgs& a, cudaStream_t stream) 
   auto kern = k_compress<U, R>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
   // for this launch shape (smem depends only on the row width).
-  static int occ_cache[64] = {0};
+  static std::atomic<int> occ_cache[64];  // per device, any host thread
   static size_t occ_smem[64] = {0};
   const int dev = plan->device;
   if (dev < 0 || dev >= 64) return IBP_EINVAL;
-  int occ = occ_cache[dev];
+  int occ = occ_cache[dev].load(std::memory_order_relaxed);
   if (occ == 0 || occ_smem[dev] != smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
@@ -203,7 +203,7 @@ static int launch_t(const ibp_plan* plan, CompressArgs& a, cudaStream_t stream) 
       cudaGetLastError();
       return IBP_ECUDA;
     }
-    occ_cache[dev] = occ;
+    occ_cache[dev].store(occ, std::memory_order_relaxed);
     occ_smem[dev] = smem;
   }
   const uint64_t blocks32 = (a.n_rows + 31) / 32;

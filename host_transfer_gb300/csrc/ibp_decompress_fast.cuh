@@ -388,10 +388,10 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
   auto kern = k_decompress_fast<R, SC, NPL, TAB, PK, GW, MP, DEV, NP, SHORT>;
   // One-time set-up per device: the shared-memory opt-in and the occupancy
   // for this launch shape.
-  static int occ_cache[64] = {0};
+  static std::atomic<int> occ_cache[64];  // per device, any host thread
   const int dev = plan->device;
   if (dev < 0 || dev >= 64) return IBP_EINVAL;
-  int occ = occ_cache[dev];
+  int occ = occ_cache[dev].load(std::memory_order_relaxed);
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     // Row-reuse copies are served from L1: prefer a quarter of the SM's
@@ -406,7 +406,7 @@ static int launch_fast_t(const ibp_plan* plan, DecodeArgs& a, cudaStream_t strea
       cudaGetLastError();
       return IBP_ECUDA;
     }
-    occ_cache[dev] = occ;
+    occ_cache[dev].store(occ, std::memory_order_relaxed);
   }
   const uint64_t groups = ((MP ? a.rows_per_plan : a.n_out) * NP + F::G - 1) / F::G;
   const uint64_t need = (groups + warps - 1) / warps;

@@ -39,7 +39,8 @@ static NoallocEntry g_noalloc[64] = {};
 // point (the library does not link the driver library itself).
 static int current_ctx_id(unsigned long long* id) {
   using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
-  static CtxGetId fn = nullptr;
+  static std::atomic<CtxGetId> fn_cache{nullptr};  // looked up once, any host thread
+  CtxGetId fn = fn_cache.load(std::memory_order_acquire);
   if (!fn) {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -50,6 +51,7 @@ static int current_ctx_id(unsigned long long* id) {
       return IBP_ECUDA;
     }
     fn = reinterpret_cast<CtxGetId>(f);
+    fn_cache.store(fn, std::memory_order_release);
   }
   if (fn(nullptr, id) != CUDA_SUCCESS) {
     set_detail("cuCtxGetId: no current context");
