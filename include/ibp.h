@@ -66,7 +66,8 @@
 extern "C" {
 #endif
 
-#define IBP_VERSION 2
+/* 3: ibp_plan_info.short_rows, ibp_get_status_async, IBP_HINT_EARLY_FETCH */
+#define IBP_VERSION 3
 #define IBP_MAX_W 8192u
 #define IBP_NOALLOC_MAX_W 4096u
 
